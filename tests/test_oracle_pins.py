@@ -1,0 +1,412 @@
+"""Pins of the double-precision oracle to facts outside itself (CPU only).
+
+Each test checks the oracle against one of: a library routine on a special case
+(torch float64 scaled_dot_product_attention, numpy / torch dtype conversions), a
+closed form, an invariant the operator contracts fix, or an example stated on the
+documentation pages (tests/golden/contract_examples.json).
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+from torch.nn.attention.bias import causal_lower_right
+
+import oracle
+from oracle import Problem
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "contract_examples.json")
+
+
+def rnd(*shape, seed=0, dtype=torch.float64, std=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g, dtype=torch.float64) * std).to(dtype)
+
+
+def run(q, k, v, **kw):
+    return oracle.attention(Problem(q=q, k=k, v=v, **kw))
+
+
+def sdpa(q, k, v, **kw):
+    return F.scaled_dot_product_attention(q.double(), k.double(), v.double(), **kw).numpy()
+
+
+# ---------------------------------------------------------------- element conversions
+
+def test_f16_widening_all_bit_patterns():
+    bits = torch.arange(0, 1 << 16, dtype=torch.int32).to(torch.int16)
+    got = oracle.to_double(oracle.F16, bits.view(torch.float16))
+    want = bits.numpy().view(np.float16).astype(np.float64)
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    np.testing.assert_array_equal(got[ok], want[ok])
+
+
+def test_bf16_widening_all_bit_patterns():
+    bits = torch.arange(0, 1 << 16, dtype=torch.int32).to(torch.int16)
+    got = oracle.to_double(oracle.BF16, bits.view(torch.bfloat16))
+    want = bits.view(torch.bfloat16).to(torch.float64).numpy()
+    np.testing.assert_array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    np.testing.assert_array_equal(got[ok], want[ok])
+
+
+def _rounding_samples():
+    g = np.random.default_rng(7)
+    mags = np.concatenate([
+        g.standard_normal(20000),
+        g.standard_normal(5000) * 1e-6,       # f16 subnormal range
+        g.standard_normal(5000) * 1e4,        # near the f16 overflow
+        g.standard_normal(2000) * 1e-40,      # binary32/bf16 subnormal range
+        g.standard_normal(2000) * 1e38,
+    ])
+    with np.errstate(over="ignore"):
+        mags = mags.astype(np.float32)
+    # exact ties between two neighbouring f16 / bf16 values
+    base16 = g.standard_normal(3000).astype(np.float16).astype(np.float32)
+    ties16 = (base16 + np.spacing(base16.astype(np.float16)).astype(np.float32) / 2).astype(np.float32)
+    return np.concatenate([mags, ties16, np.float32([0.0, -0.0, 65504, 65519, 65520, 65536, 1e-8])])
+
+
+def test_f16_rounding_matches_numpy():
+    xs = _rounding_samples()
+    with np.errstate(over="ignore"):
+        want = xs.astype(np.float16).view(np.uint16)
+    got = np.array([oracle.round_f16(float(x)) for x in xs], dtype=np.uint16)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(float(xs[i]), hex(got[i]), hex(want[i])) for i in bad[:5]]
+
+
+def test_bf16_rounding_matches_torch():
+    xs = _rounding_samples()
+    want = torch.from_numpy(xs).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = np.array([oracle.round_bf16(float(x)) for x in xs], dtype=np.uint16)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, [(float(xs[i]), hex(got[i]), hex(want[i])) for i in bad[:5]]
+
+
+# ---------------------------------------------------------------- library special cases
+
+@pytest.mark.parametrize("shape", [(1, 2, 16, 16, 8), (2, 3, 5, 9, 16), (1, 1, 1, 7, 4)])
+def test_plain_attention_equals_torch_sdpa(shape):
+    B, N, S, T, H = shape
+    q, k, v = rnd(B, N, S, H, seed=1), rnd(B, N, T, H, seed=2), rnd(B, N, T, H, seed=3)
+    np.testing.assert_allclose(run(q, k, v), sdpa(q, k, v), rtol=0, atol=1e-12)
+
+
+def test_explicit_scale_and_value_width():
+    q, k, v = rnd(2, 2, 6, 8, seed=4), rnd(2, 2, 9, 8, seed=5), rnd(2, 2, 9, 5, seed=6)
+    np.testing.assert_allclose(run(q, k, v, scale=0.37), sdpa(q, k, v, scale=0.37), atol=1e-12)
+
+
+@pytest.mark.parametrize("S,T", [(7, 7), (4, 9), (9, 4)])
+def test_upper_left_causal_equals_torch_is_causal(S, T):
+    q, k, v = rnd(1, 2, S, 8, seed=7), rnd(1, 2, T, 8, seed=8), rnd(1, 2, T, 8, seed=9)
+    got = run(q, k, v, causal=oracle.CAUSAL_UPPER_LEFT)
+    want = sdpa(q, k, v, is_causal=True)
+    rows_ok = np.isfinite(want).all(axis=-1)            # torch gives NaN on empty rows
+    np.testing.assert_allclose(got[rows_ok], want[rows_ok], atol=1e-12)
+    np.testing.assert_array_equal(got[~rows_ok], 0.0)     # reading: empty row -> zeros
+
+
+def test_lower_right_causal_with_past_equals_torch_causal_lower_right():
+    B, N, S, P, H = 2, 2, 3, 5, 8
+    q = rnd(B, N, S, H, seed=10)
+    past_k, past_v = rnd(B, N, P, H, seed=11), rnd(B, N, P, H, seed=12)
+    k, v = rnd(B, N, S, H, seed=13), rnd(B, N, S, H, seed=14)
+    got = run(q, k, v, past_k=past_k, past_v=past_v, causal=oracle.CAUSAL_LOWER_RIGHT)
+    kt, vt = torch.cat([past_k, k], 2), torch.cat([past_v, v], 2)
+    want = sdpa(q, kt, vt, attn_mask=causal_lower_right(S, P + S))
+    np.testing.assert_allclose(got, want, atol=1e-12)
+
+
+def test_bool_and_float_masks_equal_torch():
+    B, N, S, T, H = 2, 3, 5, 7, 8
+    q, k, v = rnd(B, N, S, H, seed=15), rnd(B, N, T, H, seed=16), rnd(B, N, T, H, seed=17)
+    g = torch.Generator().manual_seed(18)
+    keep = torch.rand(B, 1, S, T, generator=g) < 0.7
+    keep[..., 0] = True
+    got = run(q, k, v, keep_mask=keep.to(torch.uint8).expand(B, N, S, T), keep_kind=oracle.KEEP_BOOL)
+    np.testing.assert_allclose(got, sdpa(q, k, v, attn_mask=keep), atol=1e-12)
+    fm = rnd(1, N, S, T, seed=19)
+    got = run(q, k, v, add_mask=fm.expand(B, N, S, T))
+    np.testing.assert_allclose(got, sdpa(q, k, v, attn_mask=fm), atol=1e-12)
+
+
+def test_grouped_heads_equal_torch_enable_gqa():
+    B, Nq, Nkv, S, T, H = 2, 8, 2, 5, 6, 16
+    q, k, v = rnd(B, Nq, S, H, seed=20), rnd(B, Nkv, T, H, seed=21), rnd(B, Nkv, T, H, seed=22)
+    np.testing.assert_allclose(run(q, k, v), sdpa(q, k, v, enable_gqa=True), atol=1e-12)
+
+
+@pytest.mark.parametrize("kind", ["nonpad", "keylen", "seqlens_k"])
+def test_length_vectors_equal_sliced_torch(kind):
+    B, N, S, T, H = 3, 2, 4, 10, 8
+    q, k, v = rnd(B, N, S, H, seed=23), rnd(B, N, T, H, seed=24), rnd(B, N, T, H, seed=25)
+    n = [1, 6, 10]
+    if kind == "nonpad":
+        lens, code = torch.tensor(n, dtype=torch.int64), oracle.LEN_NONPAD_I64
+    elif kind == "keylen":
+        lens, code = torch.tensor(n, dtype=torch.int32), oracle.LEN_KEYLEN_I32
+    else:
+        lens, code = torch.tensor([x - 1 for x in n], dtype=torch.int32), oracle.LEN_SEQLENS_K_I32
+    got = run(q, k, v, lens=lens, len_kind=code)
+    for b in range(B):
+        want = sdpa(q[b:b + 1], k[b:b + 1, :, :n[b]], v[b:b + 1, :, :n[b]])
+        np.testing.assert_allclose(got[b:b + 1], want, atol=1e-12)
+
+
+def test_projection_bias_segments_equal_torch_on_biased_inputs():
+    B, N, S, T, H, Hv = 2, 2, 4, 6, 8, 4
+    q, k, v = rnd(B, N, S, H, seed=26), rnd(B, N, T, H, seed=27), rnd(B, N, T, Hv, seed=28)
+    bias = rnd(2 * N * H + N * Hv, seed=29)
+    qb, kb, vb = bias[:N * H], bias[N * H:2 * N * H], bias[2 * N * H:]
+    got = run(q, k, v, q_bias=qb, k_bias=kb, v_bias=vb)
+    want = sdpa(q + qb.view(1, N, 1, H), k + kb.view(1, N, 1, H), v + vb.view(1, N, 1, Hv))
+    np.testing.assert_allclose(got, want, atol=1e-12)
+
+
+# ---------------------------------------------------------------- present outputs
+
+def test_present_holds_past_then_new_bit_exact():
+    cases = json.load(open(GOLDEN))["present_positions"]["cases"]
+    for c in cases:
+        P, L = c["P"] if c["P"] < 100 else 9, c["L"]
+        past = rnd(2, 3, P, 8, seed=30, dtype=torch.float16) if P else None
+        cur = rnd(2, 3, L, 8, seed=31, dtype=torch.float16)
+        pres = oracle.present(past, cur)
+        assert pres.shape[2] == P + L
+        if P:
+            assert torch.equal(pres[:, :, :P].view(torch.int16), past.view(torch.int16))
+        assert torch.equal(pres[:, :, P:].view(torch.int16), cur.view(torch.int16))
+
+
+def test_present_with_bias_rounds_once():
+    cur = rnd(2, 3, 5, 8, seed=32, dtype=torch.float16)
+    bias = rnd(3 * 8, seed=33, dtype=torch.float16, std=0.02)
+    pres = oracle.present(None, cur, bias)
+    exact = cur.double().numpy() + bias.double().numpy().reshape(1, 3, 1, 8)
+    want = exact.astype(np.float16)                      # numpy rounds float64 -> float16 once
+    np.testing.assert_array_equal(pres.numpy().view(np.uint16), want.view(np.uint16))
+    curb = rnd(2, 3, 5, 8, seed=34, dtype=torch.bfloat16)
+    biasb = rnd(3 * 8, seed=35, dtype=torch.bfloat16, std=0.02)
+    presb = oracle.present(None, curb, biasb)
+    sum32 = curb.float() + biasb.float().view(1, 3, 1, 8)  # exact in binary32 at these magnitudes
+    assert torch.equal(sum32.double(), curb.double() + biasb.double().view(1, 3, 1, 8))
+    assert torch.equal(presb.view(torch.int16), sum32.to(torch.bfloat16).view(torch.int16))
+
+
+# ---------------------------------------------------------------- closed forms
+
+def test_identical_keys_give_mean_of_admitted_values():
+    B, N, S, T, H, Hv = 2, 2, 6, 11, 8, 3
+    q = rnd(B, N, S, H, seed=36)
+    k = rnd(1, 1, 1, H, seed=37).expand(B, N, T, H).contiguous()
+    v = rnd(B, N, T, Hv, seed=38)
+    lens = torch.tensor([7, 11], dtype=torch.int64)
+    got = run(q, k, v, causal=oracle.CAUSAL_LOWER_RIGHT, window=3,
+              lens=lens, len_kind=oracle.LEN_NONPAD_I64)
+    for b in range(B):
+        for i in range(S):
+            pos = T - S + i
+            adm = [j for j in range(T) if j <= pos and j >= pos - 2 and j < lens[b]]
+            want = v[b, :, adm].mean(dim=1).numpy() if adm else np.zeros((N, Hv))
+            np.testing.assert_allclose(got[b, :, i], want, atol=1e-12)
+
+
+def test_window_example_from_the_pages():
+    ex = json.load(open(GOLDEN))["local_window_example"]
+    W, before = ex["local_window_size"], ex["preceding_positions_attended"]
+    T = W + 52
+    q = torch.zeros(1, 1, T, 1, dtype=torch.float64)
+    k = torch.zeros(1, 1, T, 1, dtype=torch.float64)
+    v = torch.arange(T, dtype=torch.float64).view(1, 1, T, 1)
+    got = run(q, k, v, causal=oracle.CAUSAL_UPPER_LEFT, window=W)
+    for i in (0, 100, W - 1, W, T - 1):
+        lo = max(0, i - before)
+        assert got[0, 0, i, 0] == pytest.approx((lo + i) / 2, abs=1e-9)
+
+
+def test_window_of_one_returns_the_current_value():
+    q, k, v = rnd(1, 2, 5, 8, seed=39), rnd(1, 2, 9, 8, seed=40), rnd(1, 2, 9, 4, seed=41)
+    got = run(q, k, v, causal=oracle.CAUSAL_LOWER_RIGHT, window=1)
+    for i in range(5):
+        np.testing.assert_allclose(got[0, :, i], v[0, :, 4 + i].numpy(), atol=1e-12)
+
+
+def test_single_admitted_key_returns_its_value():
+    q, k, v = rnd(2, 2, 3, 8, seed=42), rnd(2, 2, 6, 8, seed=43), rnd(2, 2, 6, 5, seed=44)
+    got = run(q, k, v, lens=torch.tensor([1, 1], dtype=torch.int64), len_kind=oracle.LEN_NONPAD_I64)
+    np.testing.assert_allclose(got, v[:, :, :1].expand(2, 2, 3, 5).numpy(), atol=1e-12)
+
+
+def test_head_sink_closed_form():
+    # n admitted keys, all scores 0, values 1: y = n / (n + e^sink); sink = ln n gives 1/2.
+    n, T = 6, 9
+    q = torch.zeros(1, 3, 1, 4, dtype=torch.float64)
+    k = torch.zeros(1, 3, T, 4, dtype=torch.float64)
+    v = torch.ones(1, 3, T, 1, dtype=torch.float64)
+    sink = torch.tensor([math.log(n), 0.0, 2.5], dtype=torch.float64)
+    got = run(q, k, v, head_sink=sink, lens=torch.tensor([n], dtype=torch.int64),
+              len_kind=oracle.LEN_NONPAD_I64)
+    assert got[0, 0, 0, 0] == pytest.approx(0.5, abs=1e-14)
+    assert got[0, 1, 0, 0] == pytest.approx(n / (n + 1.0), abs=1e-14)
+    assert got[0, 2, 0, 0] == pytest.approx(n / (n + math.exp(2.5)), abs=1e-14)
+
+
+def _softcap_two_keys(add_first=0.0, raw_first=None, **kw):
+    # c = 2 ln 3 and a raw score c*atanh(1/2) = (ln 3)^2 cap to c/2 = ln 3: weights 3/4, 1/4.
+    c = 2 * math.log(3.0)
+    raw = (math.log(3.0) ** 2) if raw_first is None else raw_first
+    q = torch.ones(1, 1, 1, 1, dtype=torch.float64)
+    k = torch.tensor([raw, 0.0], dtype=torch.float64).view(1, 1, 2, 1)
+    v = torch.tensor([1.0, 0.0], dtype=torch.float64).view(1, 1, 2, 1)
+    mask = torch.tensor([add_first, 0.0], dtype=torch.float64).view(1, 1, 1, 2)
+    return run(q, k, v, scale=1.0, softcap=c, add_mask=mask, **kw)[0, 0, 0, 0], c
+
+
+def test_softcap_closed_form():
+    y, _ = _softcap_two_keys()
+    assert y == pytest.approx(0.75, abs=1e-14)
+
+
+def test_bias_enters_before_softcap_in_the_stage_order():
+    # raw score 0 with a finite bias (ln 3)^2: bias-then-cap gives ln 3 -> 3/4;
+    # cap-then-bias gives (ln 3)^2 -> e^{(ln3)^2} / (1 + e^{(ln3)^2}).
+    b = math.log(3.0) ** 2
+    y, _ = _softcap_two_keys(add_first=b, raw_first=0.0)
+    assert y == pytest.approx(0.75, abs=1e-14)
+    y2, _ = _softcap_two_keys(add_first=b, raw_first=0.0, softcap_before_bias=True)
+    assert y2 == pytest.approx(math.exp(b) / (1 + math.exp(b)), abs=1e-14)
+
+
+def test_negative_infinite_mask_entry_stays_excluded_under_softcap():
+    y, _ = _softcap_two_keys(add_first=-math.inf)
+    assert y == 0.0
+
+
+# ---------------------------------------------------------------- invariants
+
+def test_gqa_equals_mha_with_repeated_kv_heads():
+    B, Nq, Nkv, S, T, H = 2, 6, 3, 5, 8, 8
+    q, k, v = rnd(B, Nq, S, H, seed=45), rnd(B, Nkv, T, H, seed=46), rnd(B, Nkv, T, H, seed=47)
+    sink = rnd(Nq, seed=48)
+    kw = dict(causal=oracle.CAUSAL_LOWER_RIGHT, window=4, head_sink=sink, softcap=3.0)
+    g = Nq // Nkv
+    a = run(q, k, v, **kw)
+    b = run(q, k.repeat_interleave(g, 1), v.repeat_interleave(g, 1), **kw)
+    np.testing.assert_allclose(a, b, atol=0)
+
+
+def test_window_wider_than_sequence_equals_full_causal():
+    q, k, v = rnd(1, 2, 7, 8, seed=49), rnd(1, 2, 7, 8, seed=50), rnd(1, 2, 7, 8, seed=51)
+    for causal in (oracle.CAUSAL_UPPER_LEFT, oracle.CAUSAL_LOWER_RIGHT):
+        a = run(q, k, v, causal=causal, window=7)
+        b = run(q, k, v, causal=causal, window=1 << 30)
+        c = run(q, k, v, causal=causal)
+        np.testing.assert_array_equal(a, c)
+        np.testing.assert_array_equal(b, c)
+
+
+def test_sink_minus_infinity_is_no_sink_and_large_sink_drives_output_to_zero():
+    q, k, v = rnd(1, 2, 4, 8, seed=52), rnd(1, 2, 6, 8, seed=53), rnd(1, 2, 6, 8, seed=54)
+    none = run(q, k, v)
+    ninf = run(q, k, v, head_sink=torch.full((2,), -math.inf, dtype=torch.float64))
+    np.testing.assert_array_equal(none, ninf)
+    big = run(q, k, v, head_sink=torch.full((2,), 200.0, dtype=torch.float64))
+    assert np.abs(big).max() < 1e-60
+    mid = run(q, k, v, head_sink=torch.full((2,), 0.5, dtype=torch.float64))
+    assert (np.abs(mid) < np.abs(none) + 1e-15).all()    # weights sum below one, same direction
+
+
+def test_softcap_zero_is_off_and_huge_softcap_converges():
+    q, k, v = rnd(1, 2, 4, 8, seed=55), rnd(1, 2, 6, 8, seed=56), rnd(1, 2, 6, 8, seed=57)
+    off = run(q, k, v)
+    np.testing.assert_array_equal(run(q, k, v, softcap=0.0), off)
+    np.testing.assert_allclose(run(q, k, v, softcap=1e7), off, atol=1e-10)
+    capped = run(q, k, v, softcap=0.5)
+    assert np.abs(capped - off).max() > 1e-3
+
+
+def test_trivial_masks_are_no_ops_and_short_masks_are_padded():
+    B, N, S, T, H = 1, 2, 4, 7, 8
+    q, k, v = rnd(B, N, S, H, seed=58), rnd(B, N, T, H, seed=59), rnd(B, N, T, H, seed=60)
+    base = run(q, k, v)
+    ones = torch.ones(B, N, S, T, dtype=torch.uint8)
+    np.testing.assert_array_equal(run(q, k, v, keep_mask=ones, keep_kind=oracle.KEEP_BOOL), base)
+    np.testing.assert_array_equal(run(q, k, v, add_mask=torch.zeros(B, N, S, T, dtype=torch.float64)), base)
+    const = torch.full((B, N, S, T), -3.25, dtype=torch.float64)
+    np.testing.assert_allclose(run(q, k, v, add_mask=const), base, atol=1e-13)
+    # a mask of width 5 < T behaves like a full-width mask padded with false / -inf
+    short = (torch.rand(B, N, S, 5, generator=torch.Generator().manual_seed(61)) < 0.8).to(torch.uint8)
+    short[..., 0] = 1
+    padded = torch.zeros(B, N, S, T, dtype=torch.uint8)
+    padded[..., :5] = short
+    np.testing.assert_array_equal(run(q, k, v, keep_mask=short, keep_kind=oracle.KEEP_BOOL),
+                                  run(q, k, v, keep_mask=padded, keep_kind=oracle.KEEP_BOOL))
+    fshort = rnd(B, N, S, 5, seed=62)
+    fpad = torch.full((B, N, S, T), -math.inf, dtype=torch.float64)
+    fpad[..., :5] = fshort
+    np.testing.assert_array_equal(run(q, k, v, add_mask=fshort), run(q, k, v, add_mask=fpad))
+
+
+def test_binary_filter_mask_equals_key_lengths_and_uses_the_filter_value():
+    B, N, S, T, H = 2, 2, 3, 8, 8
+    q, k, v = rnd(B, N, S, H, seed=63), rnd(B, N, T, H, seed=64), rnd(B, N, T, H, seed=65)
+    lens = torch.tensor([3, 8], dtype=torch.int32)
+    binm = (torch.arange(T).view(1, T) < lens.view(B, 1)).to(torch.int32).view(B, 1, 1, T)
+    a = run(q, k, v, lens=lens, len_kind=oracle.LEN_KEYLEN_I32)
+    b = run(q, k, v, keep_mask=binm.expand(B, N, S, T), keep_kind=oracle.KEEP_FILTER)
+    np.testing.assert_array_equal(a, b)
+    # every key filtered: the filter value shifts all scores equally -> unmasked softmax
+    zero = torch.zeros(B, dtype=torch.int32)
+    np.testing.assert_allclose(run(q, k, v, lens=zero, len_kind=oracle.LEN_KEYLEN_I32),
+                               run(q, k, v), atol=1e-12)
+    filt = json.load(open(GOLDEN))["mask_filter_value_default"]["value"]
+    assert Problem(q=q, k=k, v=v).mask_filter_value == filt
+
+
+def test_past_split_point_does_not_change_the_result():
+    B, N, S, T, H = 2, 2, 3, 9, 8
+    q = rnd(B, N, S, H, seed=66)
+    kt, vt = rnd(B, N, T, H, seed=67), rnd(B, N, T, H, seed=68)
+    whole = run(q, kt, vt, causal=oracle.CAUSAL_LOWER_RIGHT)
+    for P in (1, 4, T - 1):
+        got = run(q, kt[:, :, P:], vt[:, :, P:], past_k=kt[:, :, :P], past_v=vt[:, :, :P],
+                  causal=oracle.CAUSAL_LOWER_RIGHT)
+        np.testing.assert_array_equal(got, whole)
+
+
+def test_layout_views_do_not_change_the_result():
+    B, N, S, H = 2, 3, 5, 8
+    q4, k4, v4 = rnd(B, N, S, H, seed=69), rnd(B, N, S, H, seed=70), rnd(B, N, S, H, seed=71)
+    q3 = q4.permute(0, 2, 1, 3).contiguous().view(B, S, N * H)
+    k3 = k4.permute(0, 2, 1, 3).contiguous().view(B, S, N * H)
+    v3 = v4.permute(0, 2, 1, 3).contiguous().view(B, S, N * H)
+    as4 = lambda t: t.view(B, S, N, H).permute(0, 2, 1, 3)
+    np.testing.assert_array_equal(run(as4(q3), as4(k3), as4(v3)), run(q4, k4, v4))
+
+
+def test_fully_excluded_row_is_zero_and_sink_keeps_it_zero():
+    q, k, v = rnd(1, 1, 2, 4, seed=72), rnd(1, 1, 3, 4, seed=73), rnd(1, 1, 3, 4, seed=74)
+    none = torch.zeros(1, 1, 2, 3, dtype=torch.uint8)
+    np.testing.assert_array_equal(run(q, k, v, keep_mask=none, keep_kind=oracle.KEEP_BOOL), 0.0)
+    np.testing.assert_array_equal(run(q, k, v, keep_mask=none, keep_kind=oracle.KEEP_BOOL,
+                                      head_sink=torch.tensor([1.0], dtype=torch.float64)), 0.0)
+
+
+def test_projection_bias_length_matches_the_contract():
+    for c in json.load(open(GOLDEN))["projection_bias_length"]["cases"]:
+        assert 2 * c["N"] * c["H"] + c["N"] * c["Hv"] == c["length"]
+
+
+def test_oracle_rejects_window_without_causal_and_bad_groups():
+    q, k, v = rnd(1, 3, 2, 4, seed=75), rnd(1, 2, 2, 4, seed=76), rnd(1, 2, 2, 4, seed=77)
+    with pytest.raises(ValueError):
+        run(q, k, v)                                  # 3 query heads over 2 kv heads
+    q2 = rnd(1, 2, 2, 4, seed=78)
+    with pytest.raises(ValueError):
+        run(q2, k, v, window=2)
