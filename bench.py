@@ -1,0 +1,438 @@
+"""Benchmark of the attention forward path on GB300.
+
+Default: the GQA prefill workload (bf16, B=2, S=T=2048, 32 query / 8 kv heads, H=128,
+upper-left causal, softcap 30, nonpad lengths in [1024, 2048]) at N=1, printed as ONE
+JSON line on rank 0.  The other workloads are measured in the same run and reported under
+"secondary" (decode in KV GB/s).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+
+--impl reference times the double-precision CPU oracle (the only other program this
+repository has for the same computation) on bounded samples of the same workload.
+Under torchrun (N > 1) every rank runs an independent replica of the workload on its
+own GPU (the path needs no exchange between GPUs; scaling is weak).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from scaled_dot_product_gb300.workloads import WORKLOADS, Case, workload  # noqa: E402
+
+L2_FLUSH_BYTES = 256 << 20          # larger than the 129 MB L2
+
+
+# ------------------------------------------------------------------------------ work model
+
+def admitted_pairs_per_row(case: Case) -> np.ndarray:
+    """(B, S) count of keys each query row must attend under the structural rules
+    (causal, window, nonpad / seqlens_k exclusion).  Float masks and filter values exclude
+    nothing, so every such key counts as work."""
+    T = case.T
+    out = np.zeros((case.B, case.S), dtype=np.int64)
+    lens = case.lens.cpu().numpy().astype(np.int64) if case.lens is not None else None
+    i = np.arange(case.S, dtype=np.int64)
+    for b in range(case.B):
+        hi = np.full(case.S, T - 1, dtype=np.int64)
+        lo = np.zeros(case.S, dtype=np.int64)
+        if case.causal != "none":
+            if case.causal == "upper_left":
+                pos = i
+            else:
+                tv = lens[b] + 1 if case.len_kind == "seqlens_k" else T
+                pos = tv - case.S + i
+            hi = np.minimum(hi, pos)
+            if case.window > 0:
+                lo = np.maximum(lo, pos - case.window + 1)
+        if case.len_kind == "nonpad":
+            hi = np.minimum(hi, lens[b] - 1)
+        elif case.len_kind == "seqlens_k":
+            hi = np.minimum(hi, lens[b])
+        out[b] = np.maximum(0, hi - lo + 1)
+    return out
+
+
+def prefill_flops(case: Case) -> float:
+    return float(admitted_pairs_per_row(case).sum()) * case.Nq * 2.0 * (case.H + case.Hv)
+
+
+def decode_bytes(case: Case) -> float:
+    es = torch.tensor([], dtype=case.dtype).element_size()
+    past = case.B * case.Nkv * case.P * (case.H + case.Hv) * es
+    new = case.B * case.Nkv * case.L * (case.H + case.Hv) * es
+    present = case.B * case.Nkv * case.T * (case.H + case.Hv) * es if case.want_present else 0
+    qy = case.B * case.Nq * case.S * (case.H + case.Hv) * es
+    return float(past + new + present + qy)
+
+
+def is_decode(idx: int) -> bool:
+    return idx == 4
+
+
+# ------------------------------------------------------------------------------ helpers
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d["hbm_gbs"], d["bf16_tflops"], d.get("bf16_tflops_sustained"), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                smax.append(float(f[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[4:8]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_digest() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "scaled_dot_product_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        h.update(n.encode())
+        h.update(open(os.path.join(csrc, n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if taken on the current sources."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("source_digest") != source_digest():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------------------ native arm
+
+def time_device(fn, steps, warmup, flush_buf, barrier):
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for s in range(steps):
+        if flush_buf is not None:
+            flush_buf.fill_(s & 0xff)       # evict the inputs from L2 between timed steps
+        starts[s].record()
+        fn()
+        ends[s].record()
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - t0
+    ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
+    return ms, wall
+
+
+def measure_native(idx: int, steps: int, warmup: int, barrier, with_e2e: bool = True):
+    from scaled_dot_product_gb300 import sdpa
+    case_cpu = workload(idx)
+    case = case_cpu.to("cuda")
+    op = "decode" if is_decode(idx) else "fwd"
+    ws = sdpa.case_workspace(case, op)
+    outs = sdpa.case_outputs(case)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    run = lambda: sdpa.run_case(case, op, outputs=outs, workspace=ws)
+    run()
+    torch.cuda.synchronize()
+    kernel = sdpa.sdpa_last_kernel_name()
+    n0 = sdpa.sdpa_launch_count()
+    run()
+    torch.cuda.synchronize()
+    per_step_launches = sdpa.sdpa_launch_count() - n0
+    input_bytes = case.input_bytes()
+    use_flush = input_bytes < (129 << 20)
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms, wall = time_device(run, steps, warmup, flush if use_flush else None, barrier)
+    res = {"idx": idx, "case": case_cpu, "op": op, "kernel": kernel, "ms": ms, "wall": wall,
+           "launches": per_step_launches * steps, "clocks": clk.summary(), "l2_flush": use_flush}
+
+    if with_e2e:
+        # end to end through the C ABI with host buffers: pinned H2D of every input, the
+        # kernels, and D2H of every output, all inside the timed region
+        host = case_cpu
+        pinned = {}
+        for name in ("q", "k", "v", "past_k", "past_v", "q_bias", "k_bias", "v_bias", "head_sink",
+                     "add_mask", "keep_mask", "lens"):
+            t = getattr(host, name)
+            if t is not None:
+                pinned[name] = (t.contiguous().pin_memory(), getattr(case, name))
+        y_host = torch.empty(outs[0].shape, dtype=outs[0].dtype).pin_memory()
+        pres_host = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in outs[2:] if t is not None]
+        h2d = sum(h.numel() * h.element_size() for h, _ in pinned.values())
+        d2h = y_host.numel() * y_host.element_size() + sum(t.numel() * t.element_size() for t in pres_host)
+
+        def e2e_step():
+            for h, d in pinned.values():
+                d.copy_(h, non_blocking=True)
+            run()
+            y_host.copy_(outs[0], non_blocking=True)
+            for hp, dp in zip(pres_host, [t for t in outs[2:] if t is not None]):
+                hp.copy_(dp, non_blocking=True)
+        e_steps = max(3, min(steps, 10))
+        e_ms, _ = time_device(e2e_step, e_steps, 2, None, barrier)
+        res.update(e2e_ms=e_ms, h2d=h2d, d2h=d2h)
+    return res
+
+
+def metric_of(idx: int, case: Case, ms: float):
+    if is_decode(idx):
+        return decode_bytes(case) / (ms * 1e-3) / 1e9, "GB/s"
+    return prefill_flops(case) / (ms * 1e-3) / 1e12, "TFLOP/s"
+
+
+def roofline(idx: int, case: Case, res: dict, hbm, tfl, tfl_src):
+    ms = statistics.mean(res["ms"])
+    if is_decode(idx):
+        achieved = decode_bytes(case) / (ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "peak_source": f"{tfl_src} copy bandwidth",
+                "traffic": ncu_traffic(res["kernel"])}
+    achieved = prefill_flops(case) / (ms * 1e-3) / 1e12
+    return {"bound": "tensor", "achieved": achieved, "peak": tfl, "unit": "TFLOP/s",
+            "frac": achieved / tfl, "peak_source": f"{tfl_src} bf16 dense burst",
+            "traffic": ncu_traffic(res["kernel"])}
+
+
+# ------------------------------------------------------------------------------ oracle arm
+
+def oracle_sample(idx: int, target_s: float, case: Case = None):
+    """Times the oracle on a sample of query rows of workload idx, sized to ~target_s seconds."""
+    import oracle
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    from oracle_adapter import problem
+    case = case if case is not None else workload(idx)
+    pr = problem(case)
+    rng = np.random.default_rng(7)
+    counts = admitted_pairs_per_row(case)
+
+    def rows_of(n):
+        return np.stack([rng.integers(0, case.B, n), rng.integers(0, case.Nq, n),
+                         rng.integers(0, case.S, n)], -1).astype(np.int64)
+
+    probe = rows_of(64)
+    t0 = time.perf_counter()
+    _, threads = oracle.attention_rows(pr, probe)
+    dt = time.perf_counter() - t0
+    n = int(max(64, min(case.B * case.Nq * case.S, 64 * target_s / max(dt, 1e-3))))
+    rows = rows_of(n)
+    t0 = time.perf_counter()
+    _, threads = oracle.attention_rows(pr, rows)
+    secs = time.perf_counter() - t0
+    if is_decode(idx):
+        es = torch.tensor([], dtype=case.dtype).element_size()
+        # bytes the sampled rows read from the KV cache (one kv row set per sampled row)
+        work = n * case.T * (case.H + case.Hv) * es
+        value, unit = work / secs / 1e9, "GB/s"
+    else:
+        work = float(counts[rows[:, 0], rows[:, 2]].sum()) * 2.0 * (case.H + case.Hv)
+        value, unit = work / secs / 1e12, "TFLOP/s"
+    return {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+            "sample": f"{n} of {case.B * case.Nq * case.S} query rows of {case.name}, "
+                      f"{secs:.1f} s on {threads} threads", "seconds": secs}
+
+
+# ------------------------------------------------------------------------------ main
+
+def dist_setup(backend):
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return ws, rank, local
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOADS))
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    a = ap.parse_args()
+    warmup = max(3, a.warmup)
+    idx = a.workload
+
+    if a.impl == "reference":
+        ws, rank, _ = dist_setup("gloo")
+        if rank != 0:
+            return
+        case = workload(idx)
+        per_step = max(1.0, 150.0 / (a.steps + warmup))
+        for _ in range(warmup):
+            oracle_sample(idx, per_step / 4, case)
+        vals, secs, last = [], [], None
+        for _ in range(a.steps):
+            last = oracle_sample(idx, per_step, case)
+            vals.append(last["value"])
+            secs.append(last["seconds"])
+        value = statistics.mean(vals)
+        line = {"impl": "reference", "metric": metric_name(idx), "value": value, "unit": last["unit"],
+                "n_gpus": a.gpus, "steps": a.steps, "warmup": warmup,
+                "ms_per_step": 1e3 * statistics.mean(secs), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": config_of(idx, case, None),
+                "cpu_baseline": {"kind": "oracle", "cores": last["cores"], "sample": last["sample"],
+                                 "value": value, "unit": last["unit"]},
+                "e2e": {"value": value, "unit": last["unit"], "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    ws, rank, local = dist_setup("nccl")
+    torch.cuda.set_device(local)
+    if ws > 1:
+        import torch.distributed as dist
+        barrier = lambda: dist.barrier()
+    else:
+        barrier = lambda: None
+    from scaled_dot_product_gb300 import build as _b
+    if rank == 0:
+        _b.build()
+    if ws > 1:
+        barrier()
+    hbm, tfl, tfl_sus, src = peaks()
+
+    res = measure_native(idx, a.steps, warmup, barrier)
+    case = res["case"]
+    ms = statistics.mean(res["ms"])
+    e2e_ms = statistics.mean(res["e2e_ms"])
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms, e2e_ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e_ms = float(t[0]), float(t[1])
+    value, unit = metric_of(idx, case, ms)
+    e2e_value, _ = metric_of(idx, case, e2e_ms)
+    if rank != 0:
+        return
+    line = {
+        "metric": metric_name(idx), "value": value * ws, "unit": unit, "n_gpus": ws,
+        "steps": a.steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": {torch.bfloat16: "bf16", torch.float16: "f16", torch.float32: "f32"}[case.dtype],
+        "data": "synthetic (seeded, drawn in fp32 on the CPU, rounded once)",
+        "config": config_of(idx, case, res),
+        "kernel": res["kernel"],
+        "ms_p10_p90": [float(np.percentile(res["ms"], 10)), float(np.percentile(res["ms"], 90))],
+        "clocks": res["clocks"],
+        "gpu_launches": res["launches"],
+        "e2e": {"value": e2e_value * ws, "unit": unit, "h2d_bytes_per_step": res["h2d"],
+                "d2h_bytes_per_step": res["d2h"], "ms_per_step": e2e_ms},
+        "roofline": roofline(idx, case, res, hbm, tfl, src),
+        "wall_s_timed_region": res["wall"],
+    }
+    if ws == 1:
+        line["cpu_baseline"] = {k: v for k, v in oracle_sample(idx, a.cpu_seconds, case).items()
+                                if k != "seconds"}
+    if not a.no_secondary:
+        sec = []
+        for j in sorted(WORKLOADS):
+            if j == idx:
+                continue
+            r = measure_native(j, max(5, a.steps // 2), warmup, barrier, with_e2e=False)
+            m = statistics.mean(r["ms"])
+            v, u = metric_of(j, r["case"], m)
+            sec.append({"workload": r["case"].name, "value": v, "unit": u, "ms_per_step": m,
+                        "kernel": r["kernel"], "gpu_launches": r["launches"],
+                        "roofline": roofline(j, r["case"], r, hbm, tfl, src) if j != 1 else None,
+                        "l2_flush": r["l2_flush"], "clocks": r["clocks"]})
+            del r
+            torch.cuda.empty_cache()
+        line["secondary"] = sec
+    print(json.dumps(line))
+
+
+def metric_name(idx: int) -> str:
+    if is_decode(idx):
+        return "attention KV-cache GB/s (decode) vs GB300 HBM roofline"
+    return "attention TFLOP/s (prefill) vs GB300 dense tensor-core roofline"
+
+
+def config_of(idx: int, case: Case, res):
+    c = {"workload": case.name, "B": case.B, "Nq": case.Nq, "Nkv": case.Nkv, "S": case.S,
+         "T": case.T, "H": case.H, "causal": case.causal, "window": case.window,
+         "softcap": case.softcap, "lens": case.len_kind,
+         "work_per_step": (f"{decode_bytes(case):.4g} bytes" if is_decode(idx)
+                           else f"{prefill_flops(case):.4g} flop")}
+    if res is not None:
+        c["l2"] = "flushed between steps (256 MB write)" if res["l2_flush"] else "inputs larger than L2"
+    return c
+
+
+if __name__ == "__main__":
+    main()

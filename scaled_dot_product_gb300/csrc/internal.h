@@ -1,0 +1,36 @@
+// Launch functions implemented by the kernel translation units and called by api.cu.
+// Each returns cudaSuccess or the launch error; none allocates memory.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+
+#include "common.cuh"
+
+namespace sdpa {
+
+// Counts one kernel launch (reported by sdpa_launch_count()).
+void count_launch(int n = 1);
+
+// General forward (any S): one warp per query row, fp32 arithmetic, reads past and new
+// K/V rows in place (projection bias added on the fly).
+cudaError_t launch_simt_fwd(const Problem& p, sdpa_dtype dt, cudaStream_t st);
+
+// present = concat(past, cur (+bias)); bit-exact without bias.
+cudaError_t launch_kv_concat(sdpa_dtype dt, int B, int N, int P, int L, int D, const View& past,
+                             const View& cur, const void* bias, const View& present, cudaStream_t st);
+
+// Split-KV decode: partials into the workspace, then the merge kernel writes y.
+struct DecodePlan {
+  int rows_per_cta;     // query rows (group heads x S) handled by one CTA
+  int row_groups;       // ceil(group * S / rows_per_cta)
+  int nsplit;           // key chunks per (batch, kv head)
+  int64_t chunk;        // keys per chunk
+  size_t ws_bytes;      // partials: m, l and unnormalised outputs
+};
+DecodePlan plan_decode(int B, int Nq, int Nkv, int S, int64_t T, int Hv);
+cudaError_t launch_decode(const Problem& p, sdpa_dtype dt, const DecodePlan& plan, void* workspace,
+                          cudaStream_t st);
+bool decode_supported(sdpa_dtype dt, int H, int Hv);
+
+}  // namespace sdpa

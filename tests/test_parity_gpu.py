@@ -1,0 +1,205 @@
+"""GPU parity: every entry point against the double-precision oracle, element by element.
+
+Tolerances (max-abs error of the output, fp32 accumulation on the GPU): 1e-4 for fp32,
+2e-2 for fp16/bf16 outputs.  present_key/present_value must be bit-exact.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle_adapter import expected_present, problem
+from scaled_dot_product_gb300 import sdpa
+from scaled_dot_product_gb300.workloads import Case, as4d, make_case, workload
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.float32: 1e-4, torch.float16: 2e-2, torch.bfloat16: 2e-2}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _device():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA device")
+    from scaled_dot_product_gb300 import build
+    build.build()
+    torch.cuda.init()
+
+
+def y_as_bnsh(case: Case, y_store: torch.Tensor) -> np.ndarray:
+    return as4d(y_store.float().cpu(), case.q_layout, case.Nq).double().numpy()
+
+
+def run_and_compare(case: Case, op: str = "fwd", rows=None):
+    dcase = case.to("cuda")
+    ws = sdpa.case_workspace(dcase, op)
+    y, pk, pv = sdpa.run_case(dcase, op, workspace=ws)
+    torch.cuda.synchronize()
+    assert sdpa.sdpa_query_status() == sdpa.SDPA_OK
+    got = y_as_bnsh(case, y)
+    pr = problem(case)
+    tol = TOL[case.dtype]
+    if rows is None:
+        want = oracle.attention(pr)
+        err = np.abs(got - want).max() if want.size else 0.0
+    else:
+        want, _ = oracle.attention_rows(pr, rows)
+        sel = got[rows[:, 0], rows[:, 1], rows[:, 2]]
+        err = np.abs(sel - want).max() if want.size else 0.0
+    assert np.isfinite(got).all()
+    assert err <= tol, f"{case.name} [{op}] max-abs error {err:.3e} > {tol}"
+    if case.want_present:
+        ek, ev = expected_present(case)
+        assert torch.equal(pk.cpu().view(torch.int16 if case.dtype != torch.float32 else torch.int32),
+                           ek.view(torch.int16 if case.dtype != torch.float32 else torch.int32))
+        assert torch.equal(pv.cpu().view(torch.int16 if case.dtype != torch.float32 else torch.int32),
+                           ev.view(torch.int16 if case.dtype != torch.float32 else torch.int32))
+    return err, sdpa.sdpa_last_kernel_name()
+
+
+# ----------------------------------------------------------------- the five workloads, small
+
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
+def test_workload_small_fwd(idx):
+    run_and_compare(workload(idx, small=True), "fwd")
+
+
+def test_workload4_small_decode():
+    err, name = run_and_compare(workload(4, small=True), "decode")
+    assert name.startswith("decode_splitkv")
+
+
+def test_workload1_exact_config():
+    err, _ = run_and_compare(workload(1), "fwd")
+    assert err <= 1e-4
+
+
+# ----------------------------------------------------------------- randomized feature sweep
+
+def _sweep_cases():
+    rng = np.random.default_rng(2024)
+    cases = []
+    for n in range(24):
+        dtype = [torch.float16, torch.bfloat16, torch.float32][n % 3]
+        H = int(rng.choice([64, 128] if dtype != torch.float32 else [32, 64, 128]))
+        Nkv = int(rng.choice([1, 2]))
+        Nq = Nkv * int(rng.choice([1, 2, 4]))
+        B = int(rng.integers(1, 3))
+        S = int(rng.choice([1, 2, 5, 17, 130, 257]))
+        L = S if rng.random() < 0.6 else int(rng.integers(1, 300))
+        P = 0 if rng.random() < 0.5 else int(rng.integers(1, 200))
+        causal = str(rng.choice(["none", "upper_left", "lower_right"]))
+        window = int(rng.integers(1, 64)) if (causal != "none" and rng.random() < 0.5) else -1
+        T = P + L
+        kw = dict(dtype=dtype, B=B, Nq=Nq, Nkv=Nkv, S=S, L=L, P=P, H=H, seed=5000 + n,
+                  causal=causal, window=window, sink=bool(rng.random() < 0.4),
+                  softcap=float(rng.choice([0.0, 0.0, 5.0, 30.0])),
+                  q_layout=str(rng.choice(["bnsh", "bsnh"])),
+                  kv_layout=str(rng.choice(["bnsh", "bsnh"])) if P == 0 else "bnsh",
+                  want_present=bool(rng.random() < 0.4))
+        m = rng.random()
+        if m < 0.25:
+            kw.update(add_mask="float", add_mask_shape=(B, 1, S, max(1, T - int(rng.integers(0, 3)))),
+                      add_mask_range=(-2.0, 1.0))
+        elif m < 0.45:
+            kw.update(keep_kind="bool", keep_mask_shape=(1, Nq, S, T))
+        elif m < 0.55:
+            kw.update(keep_kind="filter", keep_mask_shape=(B, 1, 1, T))
+        lk = rng.random()
+        if lk < 0.2:
+            kw.update(len_kind="nonpad", len_range=(1, T))
+        elif lk < 0.35:
+            kw.update(len_kind="keylen", len_range=(1, T))
+        if rng.random() < 0.25:
+            kw.update(qkv_bias="qkv" if P == 0 or rng.random() < 0.5 else "q")
+        cases.append(make_case(f"sweep{n}", **kw))
+    return cases
+
+
+SWEEP = _sweep_cases()
+
+
+@pytest.mark.parametrize("case", SWEEP, ids=[c.name for c in SWEEP])
+def test_sweep_fwd(case):
+    run_and_compare(case, "fwd")
+
+
+@pytest.mark.parametrize("case", [c for c in SWEEP if c.S <= 16 and c.H == c.Hv and
+                                  (c.dtype != torch.float32 or c.H in (32, 64, 128))],
+                         ids=lambda c: c.name)
+def test_sweep_decode(case):
+    run_and_compare(case, "decode")
+
+
+# ----------------------------------------------------------------- edge cases
+
+def test_no_keys_gives_zeros_and_sink_keeps_zero():
+    for sink in (False, True):
+        c = make_case("nokeys", dtype=torch.float16, B=1, Nq=2, S=3, L=0, H=64, sink=sink, seed=11)
+        dcase = c.to("cuda")
+        y, _, _ = sdpa.run_case(dcase, "fwd")
+        torch.cuda.synchronize()
+        assert torch.count_nonzero(y) == 0
+
+
+def test_fully_excluded_rows_are_zero():
+    c = make_case("allmasked", dtype=torch.bfloat16, B=1, Nq=2, S=40, L=40, H=64, seed=12,
+                  keep_kind="bool", keep_mask_shape=(1, 1, 40, 40), keep_density=0.0)
+    run_and_compare(c, "fwd")
+
+
+def test_empty_batch_and_empty_query_write_present_only():
+    c = make_case("emptyq", dtype=torch.float16, B=2, Nq=2, S=0, L=5, P=3, H=64, seed=13,
+                  want_present=True)
+    run_and_compare(c, "fwd")
+    run_and_compare(c, "decode")
+
+
+def test_head_size_256_and_distinct_value_width():
+    run_and_compare(make_case("h256", dtype=torch.bfloat16, B=1, Nq=2, S=70, L=90, H=256, seed=14), "fwd")
+    run_and_compare(make_case("hv", dtype=torch.float16, B=1, Nq=4, Nkv=2, S=33, L=70, H=64, Hv=128,
+                              seed=15, causal="lower_right"), "fwd")
+
+
+def test_softcap_after_bias_reading():
+    c = make_case("capbias", dtype=torch.float32, B=1, Nq=2, S=9, L=11, H=32, seed=16, softcap=2.0,
+                  add_mask="float", add_mask_range=(-3.0, 3.0))
+    run_and_compare(c, "fwd")
+    c.softcap_before_bias = True
+    run_and_compare(c, "fwd")
+
+
+def test_kv_concat_bit_exact_with_and_without_bias():
+    for dtype in (torch.float16, torch.bfloat16, torch.float32):
+        g = torch.Generator().manual_seed(17)
+        past = torch.randn(2, 3, 37, 64, generator=g).to(dtype)
+        cur = torch.randn(2, 3, 5, 64, generator=g).to(dtype)
+        bias = (torch.randn(3 * 64, generator=g) * 0.02).to(dtype)
+        for b in (None, bias):
+            pres = torch.empty(2, 3, 42, 64, dtype=dtype, device="cuda")
+            sdpa.sdpa_kv_concat(past.cuda(), cur.cuda(), pres, None if b is None else b.cuda())
+            torch.cuda.synchronize()
+            want = oracle.present(past, cur, b)
+            iv = torch.int32 if dtype == torch.float32 else torch.int16
+            assert torch.equal(pres.cpu().view(iv), want.view(iv)), (dtype, b is not None)
+
+
+# ----------------------------------------------------------------- full-size workloads, sampled rows
+
+def _sample_rows(case: Case, n: int, seed: int) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    rows = np.stack([rng.integers(0, case.B, n), rng.integers(0, case.Nq, n),
+                     rng.integers(0, case.S, n)], -1)
+    edges = np.array([[0, 0, 0], [case.B - 1, case.Nq - 1, case.S - 1],
+                      [case.B - 1, 0, case.S - 1], [0, case.Nq - 1, min(case.S - 1, 127)],
+                      [0, 0, min(case.S - 1, 128)]])
+    return np.concatenate([rows, edges]).astype(np.int64)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("idx,op", [(2, "fwd"), (3, "fwd"), (4, "decode"), (4, "fwd"), (5, "fwd")])
+def test_workload_full_size_sampled(idx, op):
+    case = workload(idx)
+    run_and_compare(case, op, rows=_sample_rows(case, 96, 100 + idx))
