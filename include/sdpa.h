@@ -168,6 +168,28 @@ SDPA_API int sdpa_attn_fwd(const sdpa_params* p, void* workspace, size_t workspa
 SDPA_API int sdpa_attn_decode(const sdpa_params* p, void* workspace, size_t workspace_bytes,
                      sdpa_stream_t stream);
 
+/* Decode without a workspace, for callers that cannot allocate device memory: a host
+ * or plugin framework that owns the whole device memory budget and gives its extensions
+ * no allocator, or a latency-critical serving loop that cannot afford cudaMalloc's
+ * implicit device-wide synchronisation or its failure under memory pressure.  (The
+ * documentation pages have no counterpart: this is a deployment variant of
+ * sdpa_attn_decode, not part of the operator contracts.)
+ * Same semantics, arguments and rules as sdpa_attn_decode; the split partials go to a
+ * fixed 8 MiB device array inside the library instead of a caller workspace.  That array
+ * is reserved on every GPU that loads the library until the process exits.
+ *  - Limit: the partials, B*Nq*S rows x nsplit chunks x (Hv + 2) floats (each part
+ *    rounded up to 256 bytes; sdpa_workspace_size(p, SDPA_OP_DECODE) reports the figure),
+ *    must fit in 8 MiB, else SDPA_ERR_WORKSPACE is returned and nothing is launched.
+ *    E.g. 2048 rows, T = 4096, Hv = 128 need about 4.3 MiB.
+ *  - The first call on each device looks up the array's device address with that device
+ *    current; make that first call before any stream capture on the device.
+ *  - Calls no cudaMalloc, cudaFree or other allocating routine.
+ *  - Every call on a device shares the one array, which keeps the last call's contents
+ *    (nothing in it needs to start at zero: each call writes every slot it reads).  Calls
+ *    that overlap on the GPU race on it and corrupt each other's results: issue them in
+ *    order on one stream. */
+SDPA_API int sdpa_attn_decode_static(const sdpa_params* p, sdpa_stream_t stream);
+
 /* Bytes of device workspace the entry point `op` (SDPA_OP_FWD / SDPA_OP_DECODE) needs for
  * these parameters; 0 when none.  Pure host function (no CUDA call); returns 0 and sets
  * sdpa_last_error() when the parameters are invalid. */

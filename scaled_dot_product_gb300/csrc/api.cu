@@ -333,6 +333,30 @@ int sdpa_attn_decode(const sdpa_params* p, void* workspace, size_t workspace_byt
   return SDPA_OK;
 }
 
+int sdpa_attn_decode_static(const sdpa_params* p, sdpa_stream_t stream) {
+  Problem r;
+  int rc = validate(p, SDPA_OP_DECODE, &r);
+  if (rc) return rc;
+  const sdpa_dtype dt = (sdpa_dtype)p->dtype;
+  const DecodePlan plan = plan_decode(r.B, r.Nq, r.Nkv, r.S, r.T, r.Hv);
+  if (plan.ws_bytes > decode_static_scratch_bytes())
+    return fail(SDPA_ERR_WORKSPACE,
+                "decode partials need %zu bytes but the built-in scratch holds %zu; "
+                "call sdpa_attn_decode with a workspace instead", plan.ws_bytes,
+                decode_static_scratch_bytes());
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  g_error.clear();
+  const int64_t rows = (int64_t)r.B * r.Nq * r.S;
+  if (rows == 0) {
+    if (r.present_k.p) return run_concat_present(r, dt, st);
+    return SDPA_OK;
+  }
+  cudaError_t e = launch_decode_static(r, dt, plan, st);
+  if (e != cudaSuccess) return cuda_fail(e, "decode (built-in scratch) launch");
+  g_kernel = dt == SDPA_F32 ? "decode_splitkv_f32" : dt == SDPA_F16 ? "decode_splitkv_f16" : "decode_splitkv_bf16";
+  return SDPA_OK;
+}
+
 int sdpa_kv_concat(sdpa_dtype dtype, int32_t B, int32_t N, int32_t P, int32_t L, int32_t D,
                    sdpa_view past, sdpa_view cur, const void* bias, sdpa_view present, sdpa_stream_t stream) {
   if (dtype != SDPA_F32 && dtype != SDPA_F16 && dtype != SDPA_BF16) return fail(SDPA_ERR_INVALID, "dtype %d", dtype);

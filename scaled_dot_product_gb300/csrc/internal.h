@@ -33,4 +33,8 @@ cudaError_t launch_decode(const Problem& p, sdpa_dtype dt, const DecodePlan& pla
                           cudaStream_t st);
 bool decode_supported(sdpa_dtype dt, int H, int Hv);
 
+// Decode with the partials in the library's own device array (no workspace).
+size_t decode_static_scratch_bytes();
+cudaError_t launch_decode_static(const Problem& p, sdpa_dtype dt, const DecodePlan& plan, cudaStream_t st);
+
 }  // namespace sdpa

@@ -80,7 +80,7 @@ class sdpa_params(ctypes.Structure):
 
 EXPORTED = ("sdpa_attn_fwd", "sdpa_attn_decode", "sdpa_workspace_size", "sdpa_validate",
             "sdpa_kv_concat", "sdpa_query_status", "sdpa_last_error", "sdpa_last_kernel_name",
-            "sdpa_version", "sdpa_launch_count")
+            "sdpa_version", "sdpa_launch_count", "sdpa_attn_decode_static")
 
 _lib = None
 
@@ -98,6 +98,8 @@ def lib() -> ctypes.CDLL:
         L.sdpa_attn_fwd.restype = ctypes.c_int
         L.sdpa_attn_decode.argtypes = [P, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.sdpa_attn_decode.restype = ctypes.c_int
+        L.sdpa_attn_decode_static.argtypes = [P, ctypes.c_void_p]
+        L.sdpa_attn_decode_static.restype = ctypes.c_int
         L.sdpa_workspace_size.argtypes = [P, ctypes.c_int]
         L.sdpa_workspace_size.restype = ctypes.c_size_t
         L.sdpa_validate.argtypes = [P, ctypes.c_int]
@@ -250,6 +252,17 @@ def sdpa_attn_fwd(q, k, v, *, y=None, workspace=None, stream=None, **kw) -> torc
 def sdpa_attn_decode(q, k, v, *, y=None, workspace=None, stream=None, **kw) -> torch.Tensor:
     """Split-KV decode (S <= 16), same arguments as sdpa_attn_fwd."""
     return _run(lib().sdpa_attn_decode, SDPA_OP_DECODE, q, k, v, y, workspace, stream, kw)
+
+
+def sdpa_attn_decode_static(q, k, v, *, y=None, stream=None, **kw) -> torch.Tensor:
+    """Decode without a workspace (the library's built-in device scratch), for callers
+    that cannot allocate device memory; same arguments as sdpa_attn_decode otherwise.
+    Calls that overlap on the GPU share that scratch and race: keep them on one stream."""
+    if y is None:
+        y = torch.empty(q.shape[0], q.shape[1], q.shape[2], v.shape[3], dtype=q.dtype, device=q.device)
+    params, keep = make_params(q, k, v, y=y, **kw)
+    _check(lib().sdpa_attn_decode_static(ctypes.byref(params), _stream(stream)))
+    return y
 
 
 def sdpa_kv_concat(past: Optional[torch.Tensor], cur: torch.Tensor, present: torch.Tensor,
