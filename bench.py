@@ -322,7 +322,9 @@ def main():
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOADS))
     ap.add_argument("--no-secondary", action="store_true")
-    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cpu-seconds", type=float, default=10.0,
+                    help="CPU work for the oracle baseline sample; 0 skips it")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     a = ap.parse_args()
     warmup = max(3, a.warmup)
     idx = a.workload
@@ -367,10 +369,10 @@ def main():
         barrier()
     hbm, tfl, tfl_sus, src = peaks()
 
-    res = measure_native(idx, a.steps, warmup, barrier)
+    res = measure_native(idx, a.steps, warmup, barrier, with_e2e=not a.no_e2e)
     case = res["case"]
     ms = statistics.mean(res["ms"])
-    e2e_ms = statistics.mean(res["e2e_ms"])
+    e2e_ms = statistics.mean(res["e2e_ms"]) if "e2e_ms" in res else float("nan")
     if ws > 1:
         import torch.distributed as dist
         t = torch.tensor([ms, e2e_ms], device="cuda")
@@ -391,12 +393,12 @@ def main():
         "ms_p10_p90": [float(np.percentile(res["ms"], 10)), float(np.percentile(res["ms"], 90))],
         "clocks": res["clocks"],
         "gpu_launches": res["launches"],
-        "e2e": {"value": e2e_value * ws, "unit": unit, "h2d_bytes_per_step": res["h2d"],
-                "d2h_bytes_per_step": res["d2h"], "ms_per_step": e2e_ms},
+        "e2e": ({"value": e2e_value * ws, "unit": unit, "h2d_bytes_per_step": res["h2d"],
+                 "d2h_bytes_per_step": res["d2h"], "ms_per_step": e2e_ms} if "e2e_ms" in res else None),
         "roofline": roofline(idx, case, res, hbm, tfl, src),
         "wall_s_timed_region": res["wall"],
     }
-    if ws == 1:
+    if ws == 1 and a.cpu_seconds > 0:
         line["cpu_baseline"] = {k: v for k, v in oracle_sample(idx, a.cpu_seconds, case).items()
                                 if k != "seconds"}
     if not a.no_secondary:

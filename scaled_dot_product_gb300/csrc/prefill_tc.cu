@@ -14,8 +14,7 @@
 // The two softmax warpgroups alternate with the tensor core: while one works on its
 // scores the MMA warp computes the other's products.  Running maxima are kept in the
 // base-2 domain and only moved (with a rescale of the TMEM accumulator) when they grow
-// by more than 2^8, so most tiles skip the rescale.  P is written to shared memory in
-// the K-major 128-byte-swizzled layout the second MMA reads.
+// by more than 2^8, so most tiles skip the rescale.
 //
 // Every barrier wait is bounded: on expiry the kernel raises an abort flag, drains the
 // copies and MMAs it issued, frees its tensor memory and records SDPA_ERR_TIMEOUT in a
@@ -40,7 +39,8 @@ using namespace ptx;
 
 constexpr int kBM = 128;        // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;        // keys per tile
-constexpr int kThreads = 384;   // 12 warps
+constexpr int kThreads = 640;   // 20 warps: 4 control + 16 softmax (4 warpgroups)
+constexpr int kHalf = kBN / 2;  // score columns per softmax thread
 constexpr float kRescaleThreshold = 8.f;   // log2 units
 
 template <int H>
@@ -49,13 +49,17 @@ struct Cfg {
   static constexpr int kRegionBytes = 128 * 128;       // 128 rows x 128 bytes
   static constexpr int kQTile = kBM * H * 2;
   static constexpr int kKVTile = kBN * H * 2;
-  static constexpr int kStages = (H == 128) ? 3 : 6;
-  static constexpr int kPTile = kBM * kBN * 2;
+  static constexpr int kStages = (H == 128) ? 4 : 10;
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = 2 * kQTile;
-  static constexpr int kPOff = kKVOff + kStages * kKVTile;
-  static constexpr int kSmem = kPOff + 2 * kPTile + 1024;   // + alignment slack
+  static constexpr int kSmem = kKVOff + kStages * kKVTile + 1024;   // + alignment slack
+  // Tensor memory (512 columns).  H = 128: S_A, S_B, O_A, O_B fill it, so P_X (16-bit,
+  // two per column) overwrites the first 64 columns of S_X once S_X is in registers.
+  // H = 64: P_A and P_B get columns of their own.
+  static constexpr bool kAlias = (H == 128);
   static constexpr int kTmemS0 = 0, kTmemS1 = 128, kTmemO0 = 256, kTmemO1 = 256 + H;
+  static constexpr int kTmemP0 = kAlias ? kTmemS0 : 256 + 2 * H;
+  static constexpr int kTmemP1 = kAlias ? kTmemS1 : 256 + 2 * H + 64;
   static constexpr uint32_t kTmemCols = 512;
 };
 
@@ -66,6 +70,8 @@ struct TcArgs {
   int causal, window, len_kind;
   const void* lens;
   int generic;                                      // per-element rules beyond the structural ones
+  int add_fast;                                     // additive mask only: vectorised path
+  int add_vec;                                      // bytes per mask load (2, 4, 8 or 16)
   Rules r;
   int q_ds, q_dn, q_db, kv_ds, kv_dn, kv_db;        // tensor-map dimension of seq / head / batch
   void* y;
@@ -109,23 +115,69 @@ __device__ __forceinline__ void key_bounds(const TcArgs& a, int64_t len_b, int64
   if (a.len_kind == SDPA_LEN_SEQLENS_K_I32) hi = min64(hi, len_b);
 }
 
+// Mask values of keys [k0, k0 + 32) of one row, as floats; keys >= T_mask read -inf.
+template <typename M>
+__device__ __forceinline__ void load_mask32_t(const M* row, int k0, int64_t T_mask, int vec_bytes, float* out) {
+  if ((int64_t)k0 + 32 <= T_mask) {
+    const M* p = row + k0;
+    if (vec_bytes >= 16) {
+      constexpr int per = 16 / sizeof(M);
+#pragma unroll
+      for (int v = 0; v < 32 / per; ++v) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + v);
+        const M* e = reinterpret_cast<const M*>(&u);
+#pragma unroll
+        for (int x = 0; x < per; ++x) out[v * per + x] = Elem<M>::to_f32(e[x]);
+      }
+    } else if (vec_bytes >= 8) {
+      constexpr int per = 8 / sizeof(M);
+#pragma unroll
+      for (int v = 0; v < 32 / per; ++v) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p) + v);
+        const M* e = reinterpret_cast<const M*>(&u);
+#pragma unroll
+        for (int x = 0; x < per; ++x) out[v * per + x] = Elem<M>::to_f32(e[x]);
+      }
+    } else {
+#pragma unroll
+      for (int x = 0; x < 32; ++x) out[x] = Elem<M>::to_f32(p[x]);
+    }
+  } else {
+#pragma unroll
+    for (int x = 0; x < 32; ++x) out[x] = ((int64_t)k0 + x < T_mask) ? Elem<M>::to_f32(row[k0 + x]) : -INFINITY;
+  }
+}
+
+__device__ __forceinline__ void load_mask32(const void* row, int dtype, int k0, int64_t T_mask, int vec_bytes,
+                                            float* out) {
+  if (dtype == SDPA_F16) load_mask32_t(reinterpret_cast<const __half*>(row), k0, T_mask, vec_bytes, out);
+  else if (dtype == SDPA_BF16) load_mask32_t(reinterpret_cast<const __nv_bfloat16*>(row), k0, T_mask, vec_bytes, out);
+  else load_mask32_t(reinterpret_cast<const float*>(row), k0, T_mask, vec_bytes, out);
+}
+
 __device__ __noinline__ float generic_score(const Rules& r, const RowCtx& ctx, float s_nat, int b, int h, int i,
                                             int64_t j) {
   return apply_rules(r, ctx, s_nat, b, h, i, j);
 }
 
-template <int H, bool kBF16>
+// Score-rule paths, fixed per launch.
+enum RuleMode { kPlain = 0, kAddMask = 1, kGeneric = 2 };
+
+template <int H, bool kBF16, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const TcArgs a) {
   using C = Cfg<H>;
+  using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_q, bar_qready, bar_drain;
   __shared__ __align__(8) uint64_t bar_full[C::kStages], bar_empty[C::kStages];
-  __shared__ __align__(8) uint64_t bar_s[2], bar_p[2];
+  __shared__ __align__(8) uint64_t bar_sfull[2], bar_sfree[2], bar_pfull[2], bar_odone[2], bar_turn[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
+  __shared__ float red_max[2][2][2][kBM];   // [tile parity][query tile][column half][row]
+  __shared__ float red_sum[2][2][kBM];      // [query tile][column half][row]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -150,22 +202,31 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = (hi_key >= lo_key) ? (int)(hi_key / kBN) - kv_t0 + 1 : 0;
 
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t sQ = sbase + C::kQOff, sKV = sbase + C::kKVOff, sP = sbase + C::kPOff;
+  const uint32_t sQ = sbase + C::kQOff, sKV = sbase + C::kKVOff;
   const uint32_t b_q = smem_u32(&bar_q), b_qready = smem_u32(&bar_qready), b_drain = smem_u32(&bar_drain);
   auto b_full = [&](int s) { return smem_u32(&bar_full[s]); };
   auto b_empty = [&](int s) { return smem_u32(&bar_empty[s]); };
-  auto b_s = [&](int x) { return smem_u32(&bar_s[x]); };
-  auto b_p = [&](int x) { return smem_u32(&bar_p[x]); };
+  auto b_sfull = [&](int x) { return smem_u32(&bar_sfull[x]); };
+  auto b_sfree = [&](int x) { return smem_u32(&bar_sfree[x]); };
+  auto b_pfull = [&](int x) { return smem_u32(&bar_pfull[x]); };
+  auto b_odone = [&](int x) { return smem_u32(&bar_odone[x]); };
+  auto b_turn = [&](int x) { return smem_u32(&bar_turn[x]); };
   volatile int* abortp = &abort_flag;
   constexpr uint64_t kDrainNs = 2000000000ull;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(b_q, 1);
-    mbar_init(b_qready, 2 * kBM);
+    mbar_init(b_qready, 4 * kBM);
     mbar_init(b_drain, 1);
     for (int s = 0; s < C::kStages; ++s) { mbar_init(b_full(s), 1); mbar_init(b_empty(s), 1); }
-    for (int x = 0; x < 2; ++x) { mbar_init(b_s(x), 1); mbar_init(b_p(x), kBM); }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(b_sfull(x), 1);
+      mbar_init(b_sfree(x), 2 * kBM);
+      mbar_init(b_pfull(x), 2 * kBM);
+      mbar_init(b_odone(x), 1);
+      mbar_init(b_turn(x), 2 * kBM);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -177,6 +238,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
 
+  // Ring order of the K/V tiles follows their first use by the MMA warp.  With P aliasing S
+  // (H = 128): K_0, V_0, K_1, V_1, ...  Otherwise S_X(j+1) is issued before PV_X(j), so the K
+  // tiles run one step ahead: K_0, K_1, V_0, K_2, V_1, ...
   if (warp == 0) {
     // ================================================================ TMA producer
     if (lane == 0 && n_tiles > 0) {
@@ -192,26 +256,34 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       int seq = 0;
       bool ok = true;
+      auto load = [&](const CUtensorMap* map, int tile) -> bool {
+        const int st = seq % C::kStages;
+        if (seq >= C::kStages &&
+            !mbar_wait_bounded(b_empty(st), ((seq / C::kStages) - 1) & 1, abortp, a.wait_ns))
+          return false;
+        mbar_arrive_expect_tx(b_full(st), C::kKVTile);
+        int d1, d2, d3;
+        perm_coords(a.kv_ds, a.kv_dn, a.kv_db, (kv_t0 + tile) * kBN, kvh, b, d1, d2, d3);
+        for (int r = 0; r < C::kRegions; ++r)
+          tma_load_4d(sKV + st * C::kKVTile + r * C::kRegionBytes, map, b_full(st), 64 * r, d1, d2, d3);
+        ++seq;
+        return true;
+      };
+      ok = load(&tk, 0);
       for (int j = 0; j < n_tiles && ok; ++j) {
-        for (int kind = 0; kind < 2 && ok; ++kind, ++seq) {
-          const int st = seq % C::kStages;
-          if (seq >= C::kStages) {
-            ok = mbar_wait_bounded(b_empty(st), ((seq / C::kStages) - 1) & 1, abortp, a.wait_ns);
-            if (!ok) break;
-          }
-          mbar_arrive_expect_tx(b_full(st), C::kKVTile);
-          perm_coords(a.kv_ds, a.kv_dn, a.kv_db, (kv_t0 + j) * kBN, kvh, b, c1, c2, c3);
-          for (int r = 0; r < C::kRegions; ++r)
-            tma_load_4d(sKV + st * C::kKVTile + r * C::kRegionBytes, kind == 0 ? &tk : &tv, b_full(st), 64 * r,
-                        c1, c2, c3);
+        if constexpr (C::kAlias) {
+          ok = load(&tv, j);
+          if (ok && j + 1 < n_tiles) ok = load(&tk, j + 1);
+        } else {
+          if (j + 1 < n_tiles) ok = load(&tk, j + 1);
+          if (ok) ok = load(&tv, j);
         }
       }
       if (!ok) {
         // let every copy already issued land before the CTA can exit
         mbar_wait_bounded(b_q, 0, nullptr, kDrainNs);
-        const int issued = seq;
-        for (int s = 0; s < C::kStages && s < issued; ++s) {
-          const int last = s + ((issued - 1 - s) / C::kStages) * C::kStages;
+        for (int s = 0; s < C::kStages && s < seq; ++s) {
+          const int last = s + ((seq - 1 - s) / C::kStages) * C::kStages;
           mbar_wait_bounded(b_full(s), (last / C::kStages) & 1, nullptr, kDrainNs);
         }
       }
@@ -224,63 +296,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdPV = idesc_f16(kBF16, kBM, H, true);
       const uint32_t tS[2] = {tmem + C::kTmemS0, tmem + C::kTmemS1};
       const uint32_t tO[2] = {tmem + C::kTmemO0, tmem + C::kTmemO1};
-      auto wait_full = [&](int seq) -> bool {
-        const bool ok = mbar_wait_bounded(b_full(seq % C::kStages), (seq / C::kStages) & 1, abortp, a.wait_ns);
+      const uint32_t tP[2] = {tmem + C::kTmemP0, tmem + C::kTmemP1};
+      int seq = 0;
+      auto wait_full = [&](int sq) -> bool {
+        const bool ok = mbar_wait_bounded(b_full(sq % C::kStages), (sq / C::kStages) & 1, abortp, a.wait_ns);
         tc_fence_after();
         return ok;
       };
+      // descriptors differ only in their start-address field: build them once
+      const uint64_t dQ[2] = {desc_sw128(sQ, 16, 1024), desc_sw128(sQ + C::kQTile, 16, 1024)};
+      const uint64_t dK0 = desc_sw128(sKV, 16, 1024);
+      const uint64_t dV0 = desc_sw128(sKV, C::kRegionBytes, 1024);
       auto issue_S = [&](int x, int st) {
-        const uint32_t q0 = sQ + x * C::kQTile, k0 = sKV + st * C::kKVTile;
+        const uint64_t dk = dK0 + (uint64_t)((st * C::kKVTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < H / 16; ++kk) {
-          const uint32_t off = (kk / 4) * C::kRegionBytes + (kk % 4) * 32;
-          mma_f16_ss(tS[x], desc_sw128(q0 + off, 16, 1024), desc_sw128(k0 + off, 16, 1024), kIdQK, kk > 0);
+          const uint64_t off = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
+          mma_f16_ss(tS[x], dQ[x] + off, dk + off, kIdQK, kk > 0);
         }
       };
       auto issue_PV = [&](int x, int st, bool acc) {
-        const uint32_t p0 = sP + x * C::kPTile, v0 = sKV + st * C::kKVTile;
+        const uint64_t dv = dV0 + (uint64_t)((st * C::kKVTile) >> 4);
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t aoff = (kk / 4) * C::kRegionBytes + (kk % 4) * 32;
-          mma_f16_ss(tO[x], desc_sw128(p0 + aoff, 16, 1024), desc_sw128(v0 + kk * 2048, C::kRegionBytes, 1024),
-                     kIdPV, (acc || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_f16_ts(tO[x], tP[x] + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdPV, (acc || kk > 0) ? 1u : 0u);
       };
       bool ok = mbar_wait_bounded(a.q_bias ? b_qready : b_q, 0, abortp, a.wait_ns);
       tc_fence_after();
-      if (ok) ok = wait_full(0);
+      if (ok) ok = wait_full(seq);
       if (ok) {
-        const int st0 = 0;
-        issue_S(0, st0);
-        mma_commit(b_s(0));
-        issue_S(1, st0);
-        mma_commit(b_s(1));
-        mma_commit(b_empty(st0));
+        const int st = seq % C::kStages;
+        issue_S(0, st);
+        mma_commit(b_sfull(0));
+        issue_S(1, st);
+        mma_commit(b_sfull(1));
+        mma_commit(b_empty(st));
+        ++seq;
       }
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int vseq = 2 * j + 1, kseq = 2 * j + 2;
-        const int vst = vseq % C::kStages, kst = kseq % C::kStages;
-        const bool more = j + 1 < n_tiles;
-        if (!(ok = wait_full(vseq))) break;
-        // tile A
-        if (!(ok = mbar_wait_bounded(b_p(0), j & 1, abortp, a.wait_ns))) break;
-        tc_fence_after();
-        issue_PV(0, vst, j > 0);
-        if (more) {
-          if (!(ok = wait_full(kseq))) break;
-          issue_S(0, kst);
+      if constexpr (C::kAlias) {
+        // P_X(j) lives in S_X's columns: PV_X(j) first, then S_X(j+1); one commit on
+        // sfull_X then also tells softmax X that O_X holds PV_X(j)
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          const bool more = j + 1 < n_tiles;
+          const int vst = seq % C::kStages;
+          if (!(ok = wait_full(seq))) break;
+          ++seq;
+          const int kst = seq % C::kStages;
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (!(ok = mbar_wait_bounded(b_pfull(x), j & 1, abortp, a.wait_ns))) break;
+            tc_fence_after();
+            issue_PV(x, vst, j > 0);
+            if (more) {
+              if (x == 0 && !(ok = wait_full(seq))) break;
+              issue_S(x, kst);
+            }
+            mma_commit(b_sfull(x));
+          }
+          if (!ok) break;
+          mma_commit(b_empty(vst));
+          if (more) {
+            mma_commit(b_empty(kst));
+            ++seq;
+          }
         }
-        mma_commit(b_s(0));
-        // tile B
-        if (!(ok = mbar_wait_bounded(b_p(1), j & 1, abortp, a.wait_ns))) break;
-        tc_fence_after();
-        issue_PV(1, vst, j > 0);
-        mma_commit(b_empty(vst));
-        if (more) {
-          issue_S(1, kst);
-          mma_commit(b_empty(kst));
+      } else {
+        for (int j = 0; j < n_tiles && ok; ++j) {
+          if (j + 1 < n_tiles) {
+            // S_X(j+1) as soon as softmax X has taken S_X(j) out of tensor memory
+            const int kst = seq % C::kStages;
+            if (!(ok = wait_full(seq))) break;
+            ++seq;
+            for (int x = 0; x < 2 && ok; ++x) {
+              if (!(ok = mbar_wait_bounded(b_sfree(x), j & 1, abortp, a.wait_ns))) break;
+              tc_fence_after();
+              issue_S(x, kst);
+              mma_commit(b_sfull(x));
+            }
+            if (!ok) break;
+            mma_commit(b_empty(kst));
+          }
+          const int vst = seq % C::kStages;
+          if (!(ok = wait_full(seq))) break;
+          ++seq;
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (!(ok = mbar_wait_bounded(b_pfull(x), j & 1, abortp, a.wait_ns))) break;
+            tc_fence_after();
+            issue_PV(x, vst, j > 0);
+            mma_commit(b_odone(x));
+          }
+          if (!ok) break;
+          mma_commit(b_empty(vst));
         }
-        mma_commit(b_s(1));
       }
       // every MMA this thread issued completes before the CTA frees its tensor memory
       mma_commit(b_drain);
@@ -289,9 +395,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ================================================================ softmax warpgroups
-    const int x = (warp - 4) >> 2;                  // query tile A or B
+    // Four warpgroups: (query tile A or B) x (score columns 0-63 or 64-127).  The two
+    // threads that share a row exchange their partial maxima through shared memory.
+    const int g = (warp - 4) >> 2;
+    const int x = g >> 1;                           // query tile A or B
+    const int hh = g & 1;                           // column half
     const int sub = warp & 3;                       // TMEM sub-partition of this warp
     const int row = sub * 32 + lane;                // row in the tile == TMEM lane
+    const int pair_bar = 1 + x * 4 + sub;           // named barrier of the two warps of these rows
     const int64_t i = (int64_t)m0 + x * kBM + row;  // query row
     const bool valid = i < a.S;
     int64_t lo = 1, hi = 0;
@@ -302,45 +413,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     RowCtx ctx;
     ctx.len = len_b;
     ctx.pos = pos_of(a, len_b, i);
+    const void* mrow = nullptr;
+    if (kMode == kAddMask && valid) {
+      const int esz = a.r.add_dtype == SDPA_F32 ? 4 : 2;
+      mrow = reinterpret_cast<const char*>(a.r.add) +
+             (b * a.r.add_sb + (int64_t)qh * a.r.add_sh + i * a.r.add_ss) * esz;
+    }
     const uint32_t trow = tmem + ((uint32_t)(sub * 32) << 16);
-    const uint32_t tS = trow + (x == 0 ? C::kTmemS0 : C::kTmemS1);
-    const uint32_t tO = trow + (x == 0 ? C::kTmemO0 : C::kTmemO1);
-    const uint32_t pRow = sP + x * C::kPTile + row * 128;
-    const int swz = row & 7;
+    const uint32_t tS = trow + (x == 0 ? C::kTmemS0 : C::kTmemS1) + kHalf * hh;
+    const uint32_t tO = trow + (x == 0 ? C::kTmemO0 : C::kTmemO1) + (H / 2) * hh;
+    const uint32_t tP = trow + (x == 0 ? C::kTmemP0 : C::kTmemP1) + (kHalf / 2) * hh;
+    // log2-domain factor applied inside the exponent: raw scores (plain mode) carry the
+    // scale or the softcap amplitude; the other modes produce log2-domain scores already
+    const float kfac = (kMode == kPlain) ? (a.has_softcap ? a.cap_out_log2 : a.scale_log2) : 1.f;
     bool ok = true;
 
     if (n_tiles > 0 && a.q_bias) {
-      // add the query segment of the projection bias to this row of Q in shared memory
+      // add the query segment of the projection bias to this row of Q (this thread's half
+      // of the columns) in shared memory
       ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_q, 0, abortp, a.wait_ns));
       if (ok) {
         const uint32_t qRow = sQ + x * C::kQTile + row * 128;
-        const auto* qb = reinterpret_cast<const typename std::conditional<kBF16, __nv_bfloat16, __half>::type*>(a.q_bias) +
-                         (int64_t)qh * H;
+        const T* qb = reinterpret_cast<const T*>(a.q_bias) + (int64_t)qh * H;
+        const int swz = row & 7;
 #pragma unroll
-        for (int r = 0; r < C::kRegions; ++r)
+        for (int c16 = 0; c16 < H / 16; ++c16) {   // 16-byte chunks of this thread's half
+          const int cidx = hh * (H / 16) + c16;      // chunk index within the row (8 elements each)
+          const int r = cidx >> 3, c = cidx & 7;
+          const uint32_t addr = qRow + r * C::kRegionBytes + ((c ^ swz) << 4);
+          uint32_t w[4];
+          ld_shared_v4(addr, w[0], w[1], w[2], w[3]);
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint32_t addr = qRow + r * C::kRegionBytes + ((c ^ swz) << 4);
-            uint32_t w[4];
-            ld_shared_v4(addr, w[0], w[1], w[2], w[3]);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              float lo_f, hi_f;
-              const int col = r * 64 + c * 8 + 2 * e;
-              if constexpr (kBF16) {
-                __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&w[e]);
-                lo_f = __bfloat162float(v.x) + __bfloat162float(qb[col]);
-                hi_f = __bfloat162float(v.y) + __bfloat162float(qb[col + 1]);
-                w[e] = pack_bf16x2(lo_f, hi_f);
-              } else {
-                __half2 v = *reinterpret_cast<__half2*>(&w[e]);
-                lo_f = __half2float(v.x) + __half2float(qb[col]);
-                hi_f = __half2float(v.y) + __half2float(qb[col + 1]);
-                w[e] = pack_f16x2(lo_f, hi_f);
-              }
-            }
-            st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+          for (int e = 0; e < 4; ++e) {
+            const int col = cidx * 8 + 2 * e;
+            const T* pv = reinterpret_cast<const T*>(&w[e]);
+            const float lo_f = Elem<T>::to_f32(pv[0]) + Elem<T>::to_f32(qb[col]);
+            const float hi_f = Elem<T>::to_f32(pv[1]) + Elem<T>::to_f32(qb[col + 1]);
+            w[e] = kBF16 ? pack_bf16x2(lo_f, hi_f) : pack_f16x2(lo_f, hi_f);
           }
+          st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+        }
         fence_proxy_async_smem();
       }
       mbar_arrive(b_qready);
@@ -348,36 +460,69 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     float m_use = -INFINITY, l = 0.f;
     for (int j = 0; j < n_tiles && ok; ++j) {
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_s(x), j & 1, abortp, a.wait_ns)))) break;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_sfull(x), j & 1, abortp, a.wait_ns)))) break;
       tc_fence_after();
-      uint32_t u[kBN];
+      float s[kHalf];
+      {
+        uint32_t u[kHalf];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) tmem_ld32(tS + c * 32, u + c * 32);
-      tmem_ld_wait();
-      float s[kBN];
+        for (int c = 0; c < kHalf / 32; ++c) tmem_ld32(tS + c * 32, u + c * 32);
+        tmem_ld_wait();
 #pragma unroll
-      for (int e = 0; e < kBN; ++e) s[e] = __uint_as_float(u[e]);
-      const int key0 = (kv_t0 + j) * kBN;
-      float mx = -INFINITY;
-      if (!a.generic) {
-        const bool full = (lo32 <= key0) && (key0 + kBN - 1 <= hi32);
+        for (int e = 0; e < kHalf; ++e) s[e] = __uint_as_float(u[e]);
+      }
+      if constexpr (!C::kAlias) {
+        // S_X(j) is in registers: the MMA warp may overwrite it with S_X(j+1)
+        tc_fence_before();
+        mbar_arrive(b_sfree(x));
+      }
+      // Ping-pong: the two query tiles take turns through the exponent-heavy part, so that
+      // one works while the tensor core runs the other's products.  Tile A goes first.
+      if (x == 1 || j > 0) {
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_turn(x), (x == 1 ? j : j - 1) & 1, abortp, a.wait_ns))))
+          break;
+      }
+      // keep the score arithmetic below the wait (it only touches registers)
+#pragma unroll
+      for (int e = 0; e < kHalf; ++e) asm volatile("" : "+f"(s[e]));
+
+      const int key0 = (kv_t0 + j) * kBN + kHalf * hh;
+      if constexpr (kMode == kPlain) {
         if (a.has_softcap) {
+          const uint64_t cin = f2_pack(a.cap_in, a.cap_in);
 #pragma unroll
-          for (int e = 0; e < kBN; ++e) s[e] = tanh_approx(s[e] * a.cap_in) * a.cap_out_log2;
-        } else {
-#pragma unroll
-          for (int e = 0; e < kBN; ++e) s[e] *= a.scale_log2;
+          for (int e = 0; e < kHalf; e += 2) {
+            float t0, t1;
+            f2_unpack(f2_mul(f2_pack(s[e], s[e + 1]), cin), t0, t1);
+            s[e] = tanh_approx(t0);
+            s[e + 1] = tanh_approx(t1);
+          }
         }
-        if (!full) {
+        if (!((lo32 <= key0) && (key0 + kHalf - 1 <= hi32))) {
+          const int elo = lo32 - key0, ehi = hi32 - key0;
 #pragma unroll
-          for (int e = 0; e < kBN; ++e) {
-            const int key = key0 + e;
-            s[e] = (key >= lo32 && key <= hi32) ? s[e] : -INFINITY;
+          for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
+        }
+      } else if constexpr (kMode == kAddMask) {
+        // additive mask / attention bias, then softcap (or the reverse), then the bounds
+#pragma unroll
+        for (int c = 0; c < kHalf / 32; ++c) {
+          float mv[32];
+          if (valid) load_mask32(mrow, a.r.add_dtype, key0 + c * 32, a.r.add_T, a.add_vec, mv);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float addv = valid ? mv[e] : 0.f;
+            float v = s[c * 32 + e] * a.scale;
+            if (!a.r.softcap_before_bias) v += addv;
+            if (a.has_softcap && v != -INFINITY) v = a.r.softcap * tanh_approx(v * (1.f / a.r.softcap));
+            if (a.r.softcap_before_bias) v += addv;
+            const int key = key0 + c * 32 + e;
+            s[c * 32 + e] = (key >= lo32 && key <= hi32) ? v * kLog2e : -INFINITY;
           }
         }
       } else {
 #pragma unroll
-        for (int e = 0; e < kBN; ++e) {
+        for (int e = 0; e < kHalf; ++e) {
           const int key = key0 + e;
           float v = -INFINITY;
           if (key >= lo32 && key <= hi32)
@@ -385,66 +530,105 @@ __global__ void __launch_bounds__(kThreads, 1)
           s[e] = v;
         }
       }
-#pragma unroll
-      for (int e = 0; e < kBN; ++e) mx = fmaxf(mx, s[e]);
 
-      // move the running maximum only when it grows by more than 2^8
-      const float m_new = fmaxf(m_use, mx);
+      // row maximum: this half (eight chains of three-input max), then the partner's half
+      float mx8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) mx8[k] = fmax3(s[k], s[k + 8], -INFINITY);
+#pragma unroll
+      for (int e = 16; e < kHalf; e += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], s[e + k], s[e + 8 + k]);
+      const float mx_own =
+          fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+      red_max[j & 1][x][hh][row] = mx_own;
+      named_bar_sync(pair_bar, 64);
+      const float mx = fmaxf(mx_own, red_max[j & 1][x][hh ^ 1][row]);
+
+      // move the running maximum only when it grows by more than 2^8 (both halves of a
+      // row see the same maxima, so they take the same decision)
+      const float m_tile = mx * kfac;
+      const float m_new = fmaxf(m_use, m_tile);
       const bool need = m_new > m_use + kRescaleThreshold;
       float corr = 1.f;
       if (need) {
         corr = ex2_approx(m_use - m_new);
         m_use = m_new;
       }
-      const bool dead = (m_use == -INFINITY);
-      float rowsum = 0.f;
+      // rows with nothing admitted yet get exponent -inf, hence p = 0
+      const float negm = (m_use == -INFINITY) ? -INFINITY : -m_use;
+      const uint64_t kf2 = f2_pack(kfac, kfac), nm2 = f2_pack(negm, negm);
+      uint64_t acc2[4] = {0, 0, 0, 0};
+      uint32_t pw[kHalf / 2];
 #pragma unroll
-      for (int c = 0; c < kBN / 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = dead ? 0.f : ex2_approx(s[c * 8 + 2 * e] - m_use);
-          const float p1 = dead ? 0.f : ex2_approx(s[c * 8 + 2 * e + 1] - m_use);
-          rowsum += p0 + p1;
-          w[e] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
-        }
-        st_shared_v4(pRow + (c >> 3) * C::kRegionBytes + (((c & 7) ^ swz) << 4), w[0], w[1], w[2], w[3]);
+      for (int e = 0; e < kHalf; e += 2) {
+        float z0, z1;
+        f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), kf2, nm2), z0, z1);
+        const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+        acc2[(e >> 1) & 3] = f2_add(acc2[(e >> 1) & 3], f2_pack(p0, p1));
+        pw[e >> 1] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
       }
-      l = l * corr + rowsum;
-      if (j > 0 && __any_sync(0xffffffffu, need)) {
-        // rescale this warp's rows of the accumulator (factor 1 for rows that kept their max)
-#pragma unroll
-        for (int c = 0; c < H / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
-          tmem_st32(tO + c * 32, o);
+      float r0, r1, r2, r3, r4, r5, r6, r7;
+      f2_unpack(acc2[0], r0, r1);
+      f2_unpack(acc2[1], r2, r3);
+      f2_unpack(acc2[2], r4, r5);
+      f2_unpack(acc2[3], r6, r7);
+      l = l * corr + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
+      mbar_arrive_after(b_turn(x ^ 1), l);
+
+      // PV_X(j-1) must be done: it reads P_X and accumulates into O_X (with P aliasing S,
+      // the sfull_X completion already implied it)
+      if (j > 0) {
+        if constexpr (!C::kAlias) {
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_odone(x), (j - 1) & 1, abortp, a.wait_ns)))) break;
+          tc_fence_after();
         }
-        tmem_st_wait();
+        if (__any_sync(0xffffffffu, need)) {
+          // rescale this thread's half of its row of the accumulator (factor 1 for rows
+          // that kept their maximum)
+          const uint64_t c2 = f2_pack(corr, corr);
+#pragma unroll
+          for (int c = 0; c < H / 64; ++c) {
+            uint32_t o[32];
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; e += 2) {
+              float v0, v1;
+              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), c2), v0, v1);
+              o[e] = __float_as_uint(v0);
+              o[e + 1] = __float_as_uint(v1);
+            }
+            tmem_st32(tO + c * 32, o);
+          }
+          tmem_st_wait();
+        }
       }
-      fence_proxy_async_smem();
+      // P_X(j) into tensor memory: lane = row, column c holds keys 2c and 2c+1
+      tmem_st32(tP, pw);
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(b_p(x));
+      mbar_arrive(b_pfull(x));
     }
 
     // ---- epilogue: O / (l + sink term), rounded once to the output type
-    if (ok && n_tiles > 0) ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_s(x), n_tiles & 1, abortp, a.wait_ns));
+    if (ok && n_tiles > 0) {
+      if constexpr (C::kAlias)
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_sfull(x), n_tiles & 1, abortp, a.wait_ns));
+      else
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_odone(x), (n_tiles - 1) & 1, abortp, a.wait_ns));
+    }
     if (ok) {
       tc_fence_after();
-      float denom = l;
-      if (a.head_sink && m_use != -INFINITY) {
-        float sk;
-        if constexpr (kBF16) sk = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(a.head_sink)[qh]);
-        else sk = __half2float(reinterpret_cast<const __half*>(a.head_sink)[qh]);
-        denom += ex2_approx(sk * kLog2e - m_use);
-      }
+      red_sum[x][hh][row] = l;
+      named_bar_sync(pair_bar, 64);
+      float denom = l + red_sum[x][hh ^ 1][row];
+      if (a.head_sink && m_use != -INFINITY)
+        denom += ex2_approx(Elem<T>::to_f32(reinterpret_cast<const T*>(a.head_sink)[qh]) * kLog2e - m_use);
       const float inv = (denom > 0.f && m_use != -INFINITY) ? 1.f / denom : 0.f;
-      using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
-      T* yrow = reinterpret_cast<T*>(a.y) + (int64_t)b * a.y_sb + (int64_t)qh * a.y_sh + i * a.y_ss;
+      T* yrow = reinterpret_cast<T*>(a.y) + (int64_t)b * a.y_sb + (int64_t)qh * a.y_sh + i * a.y_ss + (H / 2) * hh;
 #pragma unroll
-      for (int c = 0; c < H / 32; ++c) {
+      for (int c = 0; c < H / 64; ++c) {
         uint32_t o[32];
         if (n_tiles > 0) {
           tmem_ld32(tO + c * 32, o);
@@ -538,19 +722,28 @@ uint64_t wait_limit_ns() {
   return v;
 }
 
-template <int H, bool kBF16>
-cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TcArgs& a,
-                     int64_t units, cudaStream_t st) {
+template <int H, bool kBF16, int kMode>
+cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TcArgs& a,
+                        int64_t units, cudaStream_t st) {
   using C = Cfg<H>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, kBF16, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    C::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
-  prefill_tc_kernel<H, kBF16><<<(unsigned)units, kThreads, C::kSmem, st>>>(tq, tk, tv, a);
+  prefill_tc_kernel<H, kBF16, kMode><<<(unsigned)units, kThreads, C::kSmem, st>>>(tq, tk, tv, a);
   count_launch(1);
   return cudaGetLastError();
+}
+
+template <int H, bool kBF16>
+cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TcArgs& a,
+                     int64_t units, cudaStream_t st) {
+  if (a.generic) return launch_mode<H, kBF16, kGeneric>(tq, tk, tv, a, units, st);
+  if (a.add_fast) return launch_mode<H, kBF16, kAddMask>(tq, tk, tv, a, units, st);
+  return launch_mode<H, kBF16, kPlain>(tq, tk, tv, a, units, st);
 }
 
 }  // namespace
@@ -578,7 +771,19 @@ cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, 
   a.window = (int)p.r.window;
   a.len_kind = p.r.len_kind;
   a.lens = p.r.lens;
-  a.generic = (p.r.add != nullptr) || (p.r.keep_kind != SDPA_KEEP_NONE) || (p.r.len_kind == SDPA_LEN_KEYLEN_I32);
+  const bool other_rules = (p.r.keep_kind != SDPA_KEEP_NONE) || (p.r.len_kind == SDPA_LEN_KEYLEN_I32);
+  a.generic = other_rules;
+  a.add_fast = (p.r.add != nullptr) && !other_rules;
+  if (p.r.add != nullptr && other_rules) a.generic = 1;
+  if (a.add_fast) {
+    // widest load every mask row start allows (key offsets are multiples of 32 elements)
+    const int64_t esz = p.r.add_dtype == SDPA_F32 ? 4 : 2;
+    uint64_t g = reinterpret_cast<uintptr_t>(p.r.add) | 16u;
+    for (int64_t st : {p.r.add_sb, p.r.add_sh, p.r.add_ss})
+      if (st) g |= (uint64_t)(st * esz);
+    a.add_vec = (int)(g & (~g + 1));   // lowest set bit
+    if (a.add_vec > 16) a.add_vec = 16;
+  }
   a.r = p.r;
   a.y = const_cast<void*>(p.y.p);
   a.y_sb = p.y.sb; a.y_sh = p.y.sh; a.y_ss = p.y.ss;
