@@ -39,9 +39,32 @@ using namespace ptx;
 
 constexpr int kBM = 128;        // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;        // keys per tile
-constexpr int kThreads = 640;   // 20 warps: 4 control + 16 softmax (4 warpgroups)
-constexpr int kHalf = kBN / 2;  // score columns per softmax thread
+#ifndef SDPA_TC_SPLIT
+#define SDPA_TC_SPLIT 1
+#endif
+constexpr int kSplit = SDPA_TC_SPLIT;             // softmax threads per query row (1 or 2)
+constexpr int kThreads = 128 + 256 * kSplit;      // 4 control warps + 2 tiles x kSplit warpgroups
+constexpr int kHalf = kBN / kSplit;               // score columns per softmax thread
+// Register split (setmaxnreg): the control warpgroup shrinks to kCtlRegs, the softmax
+// warpgroups grow to kSmxRegs.  The sum must not exceed what the block was launched with
+// (kThreads x the kernel's register count), which the host checks before every launch.
+constexpr int kLaunchRegs = (65536 / kThreads) & ~7;
+constexpr int kCtlRegs = 80;
+constexpr int kSmxRegs = ((kLaunchRegs * kThreads - kCtlRegs * 128) / (256 * kSplit)) & ~7;
+static_assert(kSmxRegs <= 256 && kSmxRegs >= kLaunchRegs, "register split");
+static_assert(kCtlRegs * 128 + kSmxRegs * 256 * kSplit <= kLaunchRegs * kThreads, "register split");
 constexpr float kRescaleThreshold = 8.f;   // log2 units
+// Softcap tanh(u) on |u| <= kTanhPolyLimit uses u - u^3/3 + 2u^5/15 on the FMA pipe: the
+// alternating Taylor series' error is below its next term, 17/315 u^7 <= 3.3e-6.
+constexpr float kTanhPolyLimit = 0.25f;
+constexpr float kTanhA1 = -1.f / 3.f, kTanhA2 = 2.f / 15.f;
+
+__device__ __forceinline__ float tanh_poly(float u) {
+  const float z = u * u;
+  const float q = fmaf(z, kTanhA2, kTanhA1);
+  const float w = u * z;
+  return fmaf(w, q, u);
+}
 
 template <int H>
 struct Cfg {
@@ -176,8 +199,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) uint64_t bar_sfull[2], bar_sfree[2], bar_pfull[2], bar_odone[2], bar_turn[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  __shared__ float red_max[2][2][2][kBM];   // [tile parity][query tile][column half][row]
-  __shared__ float red_sum[2][2][kBM];      // [query tile][column half][row]
+  __shared__ float red_max[2][2][kSplit][kBM];   // [tile parity][query tile][column part][row]
+  __shared__ float red_sum[2][kSplit][kBM];      // [query tile][column part][row]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -217,15 +240,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(b_q, 1);
-    mbar_init(b_qready, 4 * kBM);
+    mbar_init(b_qready, 2 * kSplit * kBM);
     mbar_init(b_drain, 1);
     for (int s = 0; s < C::kStages; ++s) { mbar_init(b_full(s), 1); mbar_init(b_empty(s), 1); }
     for (int x = 0; x < 2; ++x) {
       mbar_init(b_sfull(x), 1);
-      mbar_init(b_sfree(x), 2 * kBM);
-      mbar_init(b_pfull(x), 2 * kBM);
+      mbar_init(b_sfree(x), kSplit * kBM);
+      mbar_init(b_pfull(x), kSplit * kBM);
       mbar_init(b_odone(x), 1);
-      mbar_init(b_turn(x), 2 * kBM);
+      mbar_init(b_turn(x), kSplit * kBM);
     }
     fence_mbar_init();
   }
@@ -237,6 +260,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
+  // the control warpgroup hands registers to the softmax warpgroups
+  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
 
   // Ring order of the K/V tiles follows their first use by the MMA warp.  With P aliasing S
   // (H = 128): K_0, V_0, K_1, V_1, ...  Otherwise S_X(j+1) is issued before PV_X(j), so the K
@@ -397,9 +422,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ softmax warpgroups
     // Four warpgroups: (query tile A or B) x (score columns 0-63 or 64-127).  The two
     // threads that share a row exchange their partial maxima through shared memory.
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSmxRegs));
     const int g = (warp - 4) >> 2;
-    const int x = g >> 1;                           // query tile A or B
-    const int hh = g & 1;                           // column half
+    const int x = g / kSplit;                       // query tile A or B
+    const int hh = g % kSplit;                      // column part
     const int sub = warp & 3;                       // TMEM sub-partition of this warp
     const int row = sub * 32 + lane;                // row in the tile == TMEM lane
     const int pair_bar = 1 + x * 4 + sub;           // named barrier of the two warps of these rows
@@ -421,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const uint32_t trow = tmem + ((uint32_t)(sub * 32) << 16);
     const uint32_t tS = trow + (x == 0 ? C::kTmemS0 : C::kTmemS1) + kHalf * hh;
-    const uint32_t tO = trow + (x == 0 ? C::kTmemO0 : C::kTmemO1) + (H / 2) * hh;
+    const uint32_t tO = trow + (x == 0 ? C::kTmemO0 : C::kTmemO1) + (H / kSplit) * hh;
     const uint32_t tP = trow + (x == 0 ? C::kTmemP0 : C::kTmemP1) + (kHalf / 2) * hh;
     // log2-domain factor applied inside the exponent: raw scores (plain mode) carry the
     // scale or the softcap amplitude; the other modes produce log2-domain scores already
@@ -437,8 +463,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const T* qb = reinterpret_cast<const T*>(a.q_bias) + (int64_t)qh * H;
         const int swz = row & 7;
 #pragma unroll
-        for (int c16 = 0; c16 < H / 16; ++c16) {   // 16-byte chunks of this thread's half
-          const int cidx = hh * (H / 16) + c16;      // chunk index within the row (8 elements each)
+        for (int c16 = 0; c16 < H / (8 * kSplit); ++c16) {   // 16-byte chunks of this thread's part
+          const int cidx = hh * (H / (8 * kSplit)) + c16;      // chunk index within the row
           const int r = cidx >> 3, c = cidx & 7;
           const uint32_t addr = qRow + r * C::kRegionBytes + ((c ^ swz) << 4);
           uint32_t w[4];
@@ -487,18 +513,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < kHalf; ++e) asm volatile("" : "+f"(s[e]));
 
       const int key0 = (kv_t0 + j) * kBN + kHalf * hh;
+      bool have_mx = false;       // set when the transform already produced this half's max
+      float mx_own = -INFINITY;
       if constexpr (kMode == kPlain) {
+        const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
         if (a.has_softcap) {
           const uint64_t cin = f2_pack(a.cap_in, a.cap_in);
 #pragma unroll
-          for (int e = 0; e < kHalf; e += 2) {
-            float t0, t1;
-            f2_unpack(f2_mul(f2_pack(s[e], s[e + 1]), cin), t0, t1);
-            s[e] = tanh_approx(t0);
-            s[e + 1] = tanh_approx(t1);
+          for (int e = 0; e < kHalf; e += 2) f2_unpack(f2_mul(f2_pack(s[e], s[e + 1]), cin), s[e], s[e + 1]);
+          bool poly = false;
+          float umax = -INFINITY;
+          if (full) {
+            float hi8[4], lo8[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) { hi8[k] = fmaxf(s[k], s[k + 4]); lo8[k] = fminf(s[k], s[k + 4]); }
+#pragma unroll
+            for (int e = 8; e < kHalf; e += 8)
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                hi8[k] = fmax3(hi8[k], s[e + k], s[e + 4 + k]);
+                lo8[k] = fminf(lo8[k], fminf(s[e + k], s[e + 4 + k]));
+              }
+            umax = fmaxf(fmaxf(hi8[0], hi8[1]), fmaxf(hi8[2], hi8[3]));
+            const float umin = fminf(fminf(lo8[0], lo8[1]), fminf(lo8[2], lo8[3]));
+            poly = fmaxf(umax, -umin) <= kTanhPolyLimit;
+          }
+          if (poly) {
+            // small arguments: odd polynomial on the FMA pipe (monotonic here, so the
+            // maximum is the polynomial of the largest argument)
+            const uint64_t a1 = f2_pack(kTanhA1, kTanhA1), a2 = f2_pack(kTanhA2, kTanhA2);
+#pragma unroll
+            for (int e = 0; e < kHalf; e += 2) {
+              const uint64_t uu = f2_pack(s[e], s[e + 1]);
+              const uint64_t z = f2_mul(uu, uu);
+              const uint64_t q = f2_fma(z, a2, a1);
+              f2_unpack(f2_fma(f2_mul(uu, z), q, uu), s[e], s[e + 1]);
+            }
+            mx_own = tanh_poly(umax);
+            have_mx = true;
+          } else {
+#pragma unroll
+            for (int e = 0; e < kHalf; ++e) s[e] = tanh_approx(s[e]);
           }
         }
-        if (!((lo32 <= key0) && (key0 + kHalf - 1 <= hi32))) {
+        if (!full) {
           const int elo = lo32 - key0, ehi = hi32 - key0;
 #pragma unroll
           for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
@@ -532,18 +590,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 
       // row maximum: this half (eight chains of three-input max), then the partner's half
-      float mx8[8];
+      if (!have_mx) {
+        float mx8[8];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) mx8[k] = fmax3(s[k], s[k + 8], -INFINITY);
+        for (int k = 0; k < 8; ++k) mx8[k] = fmax3(s[k], s[k + 8], -INFINITY);
 #pragma unroll
-      for (int e = 16; e < kHalf; e += 16)
+        for (int e = 16; e < kHalf; e += 16)
 #pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], s[e + k], s[e + 8 + k]);
-      const float mx_own =
-          fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      red_max[j & 1][x][hh][row] = mx_own;
-      named_bar_sync(pair_bar, 64);
-      const float mx = fmaxf(mx_own, red_max[j & 1][x][hh ^ 1][row]);
+          for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], s[e + k], s[e + 8 + k]);
+        mx_own = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+      }
+      float mx = mx_own;
+      if constexpr (kSplit == 2) {
+        red_max[j & 1][x][hh][row] = mx_own;
+        named_bar_sync(pair_bar, 64);
+        mx = fmaxf(mx_own, red_max[j & 1][x][hh ^ 1][row]);
+      }
 
       // move the running maximum only when it grows by more than 2^8 (both halves of a
       // row see the same maxima, so they take the same decision)
@@ -588,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // that kept their maximum)
           const uint64_t c2 = f2_pack(corr, corr);
 #pragma unroll
-          for (int c = 0; c < H / 64; ++c) {
+          for (int c = 0; c < H / (32 * kSplit); ++c) {
             uint32_t o[32];
             tmem_ld32(tO + c * 32, o);
             tmem_ld_wait();
@@ -605,7 +667,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // P_X(j) into tensor memory: lane = row, column c holds keys 2c and 2c+1
-      tmem_st32(tP, pw);
+#pragma unroll
+      for (int c = 0; c < kHalf / 64; ++c) tmem_st32(tP + c * 32, pw + c * 32);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(b_pfull(x));
@@ -620,15 +683,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (ok) {
       tc_fence_after();
-      red_sum[x][hh][row] = l;
-      named_bar_sync(pair_bar, 64);
-      float denom = l + red_sum[x][hh ^ 1][row];
+      float denom = l;
+      if constexpr (kSplit == 2) {
+        red_sum[x][hh][row] = l;
+        named_bar_sync(pair_bar, 64);
+        denom += red_sum[x][hh ^ 1][row];
+      }
       if (a.head_sink && m_use != -INFINITY)
         denom += ex2_approx(Elem<T>::to_f32(reinterpret_cast<const T*>(a.head_sink)[qh]) * kLog2e - m_use);
       const float inv = (denom > 0.f && m_use != -INFINITY) ? 1.f / denom : 0.f;
-      T* yrow = reinterpret_cast<T*>(a.y) + (int64_t)b * a.y_sb + (int64_t)qh * a.y_sh + i * a.y_ss + (H / 2) * hh;
+      T* yrow = reinterpret_cast<T*>(a.y) + (int64_t)b * a.y_sb + (int64_t)qh * a.y_sh + i * a.y_ss +
+                (H / kSplit) * hh;
 #pragma unroll
-      for (int c = 0; c < H / 64; ++c) {
+      for (int c = 0; c < H / (32 * kSplit); ++c) {
         uint32_t o[32];
         if (n_tiles > 0) {
           tmem_ld32(tO + c * 32, o);
@@ -731,6 +798,11 @@ cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   std::call_once(once, [] {
     attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, kBF16, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     C::kSmem);
+    // the in-kernel register split assumes the block is launched with kLaunchRegs per
+    // thread; with fewer, the softmax warps' request could never be met
+    cudaFuncAttributes fa{};
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<H, kBF16, kMode>);
+    if (attr_err == cudaSuccess && fa.numRegs < kLaunchRegs) attr_err = cudaErrorLaunchOutOfResources;
   });
   if (attr_err != cudaSuccess) return attr_err;
   prefill_tc_kernel<H, kBF16, kMode><<<(unsigned)units, kThreads, C::kSmem, st>>>(tq, tk, tv, a);
