@@ -178,6 +178,54 @@ __device__ __forceinline__ void load_mask32(const void* row, int dtype, int k0, 
   else load_mask32_t(reinterpret_cast<const float*>(row), k0, T_mask, vec_bytes, out);
 }
 
+// Mask values of keys [k0, k0 + 128) of one row, as 64 packed 16-bit pairs in the mask's
+// own type (element 2c in the low half of word c).  Keys >= T_mask read -inf.
+template <typename M>
+__device__ __forceinline__ void prefetch_mask128(const M* row, int k0, int64_t T_mask, int vec_bytes,
+                                                 uint32_t* raw) {
+  static_assert(sizeof(M) == 2, "16-bit masks");
+  if ((int64_t)k0 + 128 <= T_mask) {
+    const M* p = row + k0;
+    if (vec_bytes >= 16) {
+#pragma unroll
+      for (int v = 0; v < 16; ++v) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + v);
+        raw[4 * v] = u.x; raw[4 * v + 1] = u.y; raw[4 * v + 2] = u.z; raw[4 * v + 3] = u.w;
+      }
+    } else if (vec_bytes >= 8) {
+#pragma unroll
+      for (int v = 0; v < 32; ++v) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p) + v);
+        raw[2 * v] = u.x; raw[2 * v + 1] = u.y;
+      }
+    } else if (vec_bytes >= 4) {
+#pragma unroll
+      for (int v = 0; v < 64; ++v) raw[v] = __ldg(reinterpret_cast<const uint32_t*>(p) + v);
+    } else {
+      const unsigned short* h = reinterpret_cast<const unsigned short*>(p);
+#pragma unroll
+      for (int v = 0; v < 64; ++v) raw[v] = (uint32_t)__ldg(h + 2 * v) | ((uint32_t)__ldg(h + 2 * v + 1) << 16);
+    }
+  } else {
+    const unsigned short ninf = sizeof(M) == 2 && std::is_same<M, __half>::value ? 0xFC00u : 0xFF80u;
+    const unsigned short* h = reinterpret_cast<const unsigned short*>(row);
+#pragma unroll
+    for (int v = 0; v < 64; ++v) {
+      const int64_t c0 = (int64_t)k0 + 2 * v, c1 = c0 + 1;
+      const uint32_t lo = c0 < T_mask ? __ldg(h + c0) : ninf;
+      const uint32_t hi = c1 < T_mask ? __ldg(h + c1) : ninf;
+      raw[v] = lo | (hi << 16);
+    }
+  }
+}
+
+template <typename M>
+__device__ __forceinline__ float mask_elem(const uint32_t* raw, int e) {
+  const unsigned short bits = (unsigned short)((e & 1) ? (raw[e >> 1] >> 16) : (raw[e >> 1] & 0xFFFFu));
+  if constexpr (std::is_same<M, __half>::value) return __half2float(__ushort_as_half(bits));
+  else return __bfloat162float(__ushort_as_bfloat16(bits));
+}
+
 __device__ __noinline__ float generic_score(const Rules& r, const RowCtx& ctx, float s_nat, int b, int h, int i,
                                             int64_t j) {
   return apply_rules(r, ctx, s_nat, b, h, i, j);
@@ -450,8 +498,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tO = trow + (x == 0 ? C::kTmemO0 : C::kTmemO1) + (H / kSplit) * hh;
     const uint32_t tP = trow + (x == 0 ? C::kTmemP0 : C::kTmemP1) + (kHalf / 2) * hh;
     // log2-domain factor applied inside the exponent: raw scores (plain mode) carry the
-    // scale or the softcap amplitude; the other modes produce log2-domain scores already
-    const float kfac = (kMode == kPlain) ? (a.has_softcap ? a.cap_out_log2 : a.scale_log2) : 1.f;
+    // scale or the softcap amplitude, additive-mask scores are in natural units, and the
+    // generic mode produces log2-domain scores already
+    const float kfac = (kMode == kPlain) ? (a.has_softcap ? a.cap_out_log2 : a.scale_log2)
+                                         : (kMode == kAddMask ? kLog2e : 1.f);
     bool ok = true;
 
     if (n_tiles > 0 && a.q_bias) {
@@ -486,6 +536,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     float m_use = -INFINITY, l = 0.f;
     for (int j = 0; j < n_tiles && ok; ++j) {
+      uint32_t mraw[kMode == kAddMask ? kHalf / 2 : 1];
+      if constexpr (kMode == kAddMask) {
+        // fetch this row's mask values for the tile now; the wait below hides the latency
+        if (valid)
+          prefetch_mask128(reinterpret_cast<const T*>(mrow), (kv_t0 + j) * kBN, a.r.add_T, a.add_vec, mraw);
+      }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_sfull(x), j & 1, abortp, a.wait_ns)))) break;
       tc_fence_after();
       float s[kHalf];
@@ -518,7 +574,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kMode == kPlain) {
         const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
         if (a.has_softcap) {
-          const uint64_t cin = f2_pack(a.cap_in, a.cap_in);
+          const f2_t cin = f2_pack(a.cap_in, a.cap_in);
 #pragma unroll
           for (int e = 0; e < kHalf; e += 2) f2_unpack(f2_mul(f2_pack(s[e], s[e + 1]), cin), s[e], s[e + 1]);
           bool poly = false;
@@ -541,12 +597,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (poly) {
             // small arguments: odd polynomial on the FMA pipe (monotonic here, so the
             // maximum is the polynomial of the largest argument)
-            const uint64_t a1 = f2_pack(kTanhA1, kTanhA1), a2 = f2_pack(kTanhA2, kTanhA2);
+            const f2_t a1 = f2_pack(kTanhA1, kTanhA1), a2 = f2_pack(kTanhA2, kTanhA2);
 #pragma unroll
             for (int e = 0; e < kHalf; e += 2) {
-              const uint64_t uu = f2_pack(s[e], s[e + 1]);
-              const uint64_t z = f2_mul(uu, uu);
-              const uint64_t q = f2_fma(z, a2, a1);
+              const f2_t uu = f2_pack(s[e], s[e + 1]);
+              const f2_t z = f2_mul(uu, uu);
+              const f2_t q = f2_fma(z, a2, a1);
               f2_unpack(f2_fma(f2_mul(uu, z), q, uu), s[e], s[e + 1]);
             }
             mx_own = tanh_poly(umax);
@@ -562,21 +618,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
         }
       } else if constexpr (kMode == kAddMask) {
-        // additive mask / attention bias, then softcap (or the reverse), then the bounds
+        // additive mask / attention bias, then softcap (or the reverse), then the bounds;
+        // scores stay in natural units here (kfac carries log2 e)
+        if (!valid) {
 #pragma unroll
-        for (int c = 0; c < kHalf / 32; ++c) {
-          float mv[32];
-          if (valid) load_mask32(mrow, a.r.add_dtype, key0 + c * 32, a.r.add_T, a.add_vec, mv);
+          for (int e = 0; e < kHalf; ++e) mraw[e >> 1] = 0u;
+        }
+        if (!a.has_softcap) {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const float addv = valid ? mv[e] : 0.f;
-            float v = s[c * 32 + e] * a.scale;
-            if (!a.r.softcap_before_bias) v += addv;
-            if (a.has_softcap && v != -INFINITY) v = a.r.softcap * tanh_approx(v * (1.f / a.r.softcap));
-            if (a.r.softcap_before_bias) v += addv;
-            const int key = key0 + c * 32 + e;
-            s[c * 32 + e] = (key >= lo32 && key <= hi32) ? v * kLog2e : -INFINITY;
+          for (int e = 0; e < kHalf; ++e) s[e] = fmaf(s[e], a.scale, mask_elem<T>(mraw, e));
+        } else if (!a.r.softcap_before_bias) {
+          const float cin = 1.f / a.r.softcap;
+#pragma unroll
+          for (int e = 0; e < kHalf; ++e) {
+            const float v = fmaf(s[e], a.scale, mask_elem<T>(mraw, e));
+            s[e] = (v == -INFINITY) ? v : a.r.softcap * tanh_approx(v * cin);
           }
+        } else {
+#pragma unroll
+          for (int e = 0; e < kHalf; ++e)
+            s[e] = fmaf(a.r.softcap, tanh_approx(s[e] * a.cap_in), mask_elem<T>(mraw, e));
+        }
+        if (!((lo32 <= key0) && (key0 + kHalf - 1 <= hi32))) {
+          const int elo = lo32 - key0, ehi = hi32 - key0;
+#pragma unroll
+          for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
         }
       } else {
 #pragma unroll
@@ -619,8 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // rows with nothing admitted yet get exponent -inf, hence p = 0
       const float negm = (m_use == -INFINITY) ? -INFINITY : -m_use;
-      const uint64_t kf2 = f2_pack(kfac, kfac), nm2 = f2_pack(negm, negm);
-      uint64_t acc2[4] = {0, 0, 0, 0};
+      const f2_t kf2 = f2_pack(kfac, kfac), nm2 = f2_pack(negm, negm);
+      f2_t acc2[4] = {f2_zero(), f2_zero(), f2_zero(), f2_zero()};
       uint32_t pw[kHalf / 2];
 #pragma unroll
       for (int e = 0; e < kHalf; e += 2) {
@@ -648,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (__any_sync(0xffffffffu, need)) {
           // rescale this thread's half of its row of the accumulator (factor 1 for rows
           // that kept their maximum)
-          const uint64_t c2 = f2_pack(corr, corr);
+          const f2_t c2 = f2_pack(corr, corr);
 #pragma unroll
           for (int c = 0; c < H / (32 * kSplit); ++c) {
             uint32_t o[32];
@@ -845,8 +911,8 @@ cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, 
   a.lens = p.r.lens;
   const bool other_rules = (p.r.keep_kind != SDPA_KEEP_NONE) || (p.r.len_kind == SDPA_LEN_KEYLEN_I32);
   a.generic = other_rules;
-  a.add_fast = (p.r.add != nullptr) && !other_rules;
-  if (p.r.add != nullptr && other_rules) a.generic = 1;
+  a.add_fast = (p.r.add != nullptr) && !other_rules && p.r.add_dtype == (int)dt && kSplit == 1;
+  if (p.r.add != nullptr && !a.add_fast) a.generic = 1;
   if (a.add_fast) {
     // widest load every mask row start allows (key offsets are multiples of 32 elements)
     const int64_t esz = p.r.add_dtype == SDPA_F32 ? 4 : 2;

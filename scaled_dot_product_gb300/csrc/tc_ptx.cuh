@@ -36,8 +36,22 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 __device__ __forceinline__ void mbar_arrive_after(uint32_t bar, float dep) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar), "f"(dep) : "memory");
 }
+// One bounded probe of the phase; the thread may sleep in it up to kWaitHintNs (or until
+// the phase completes) instead of spinning on the issue port.
+#ifndef SDPA_WAIT_HINT_NS
+#define SDPA_WAIT_HINT_NS 0
+#endif
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
+#if SDPA_WAIT_HINT_NS > 0
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "n"(SDPA_WAIT_HINT_NS)
+      : "memory");
+#else
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
@@ -45,6 +59,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "=r"(ok)
       : "r"(bar), "r"(parity)
       : "memory");
+#endif
   return ok != 0;
 }
 
@@ -198,30 +213,46 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   return r;
 }
 
-// Paired fp32 arithmetic (two lanes of f32 in one 64-bit register).
-__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+// Paired fp32 arithmetic (two lanes of f32 in one 64-bit register: fma/add/mul .f32x2).
+// SDPA_SCALAR_F2 selects plain scalar instructions with the same results, for comparison.
+#ifndef SDPA_SCALAR_F2
+using f2_t = uint64_t;
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
   return r;
 }
-__device__ __forceinline__ void f2_unpack(uint64_t v, float& lo, float& hi) {
+__device__ __forceinline__ void f2_unpack(f2_t v, float& lo, float& hi) {
   asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
 }
-__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
   uint64_t d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
   return d;
 }
-__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) {
   uint64_t d;
   asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
-__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) {
   uint64_t d;
   asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ f2_t f2_zero() { return 0ull; }
+#else
+using f2_t = float2;
+__device__ __forceinline__ f2_t f2_pack(float lo, float hi) { return make_float2(lo, hi); }
+__device__ __forceinline__ void f2_unpack(f2_t v, float& lo, float& hi) { lo = v.x; hi = v.y; }
+__device__ __forceinline__ f2_t f2_fma(f2_t a, f2_t b, f2_t c) {
+  return make_float2(__fmaf_rn(a.x, b.x, c.x), __fmaf_rn(a.y, b.y, c.y));
+}
+__device__ __forceinline__ f2_t f2_add(f2_t a, f2_t b) { return make_float2(__fadd_rn(a.x, b.x), __fadd_rn(a.y, b.y)); }
+__device__ __forceinline__ f2_t f2_mul(f2_t a, f2_t b) { return make_float2(__fmul_rn(a.x, b.x), __fmul_rn(a.y, b.y)); }
+__device__ __forceinline__ f2_t f2_zero() { return make_float2(0.f, 0.f); }
+#endif
+
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
