@@ -193,9 +193,9 @@ def time_device(fn, steps, warmup, flush_buf, barrier):
     return ms, wall
 
 
-def measure_native(idx: int, steps: int, warmup: int, barrier, with_e2e: bool = True):
+def measure_native(idx: int, steps: int, warmup: int, barrier, with_e2e: bool = True, batch=None):
     from scaled_dot_product_gb300 import sdpa
-    case_cpu = workload(idx)
+    case_cpu = workload(idx, batch=batch)
     case = case_cpu.to("cuda")
     op = "decode" if is_decode(idx) else "fwd"
     ws = sdpa.case_workspace(case, op)
@@ -265,43 +265,64 @@ def roofline(idx: int, case: Case, res: dict, hbm, tfl, tfl_src):
 
 # ------------------------------------------------------------------------------ oracle arm
 
+class OracleSampler:
+    """Times the oracle on samples of query rows of one workload (CPU baseline / reference
+    arm).  The per-row cost is calibrated once, so every step can be sized from a budget."""
+
+    def __init__(self, idx: int, case: Case = None):
+        import oracle
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        from oracle_adapter import problem
+        self.oracle = oracle
+        self.idx = idx
+        self.case = case if case is not None else workload(idx)
+        self.pr = problem(self.case)
+        self.rng = np.random.default_rng(7)
+        self.counts = admitted_pairs_per_row(self.case)
+        t0 = time.perf_counter()
+        _, self.threads = oracle.attention_rows(self.pr, self._rows(64))
+        self.sec_per_row = max((time.perf_counter() - t0) / 64, 1e-7)
+
+    def _rows(self, n):
+        c = self.case
+        return np.stack([self.rng.integers(0, c.B, n), self.rng.integers(0, c.Nq, n),
+                         self.rng.integers(0, c.S, n)], -1).astype(np.int64)
+
+    def step(self, target_s: float):
+        c = self.case
+        n = int(max(1, min(c.B * c.Nq * c.S, target_s / self.sec_per_row)))
+        rows = self._rows(n)
+        t0 = time.perf_counter()
+        _, threads = self.oracle.attention_rows(self.pr, rows)
+        secs = time.perf_counter() - t0
+        if is_decode(self.idx):
+            es = torch.tensor([], dtype=c.dtype).element_size()
+            work = n * c.T * (c.H + c.Hv) * es        # KV-cache bytes the sampled rows read
+            value, unit = work / secs / 1e9, "GB/s"
+        else:
+            work = float(self.counts[rows[:, 0], rows[:, 2]].sum()) * 2.0 * (c.H + c.Hv)
+            value, unit = work / secs / 1e12, "TFLOP/s"
+        return {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+                "sample": f"{n} of {c.B * c.Nq * c.S} query rows of {c.name}, {secs:.2f} s on {threads} threads",
+                "seconds": secs}
+
+
 def oracle_sample(idx: int, target_s: float, case: Case = None):
-    """Times the oracle on a sample of query rows of workload idx, sized to ~target_s seconds."""
-    import oracle
-    sys.path.insert(0, os.path.join(ROOT, "tests"))
-    from oracle_adapter import problem
-    case = case if case is not None else workload(idx)
-    pr = problem(case)
-    rng = np.random.default_rng(7)
-    counts = admitted_pairs_per_row(case)
-
-    def rows_of(n):
-        return np.stack([rng.integers(0, case.B, n), rng.integers(0, case.Nq, n),
-                         rng.integers(0, case.S, n)], -1).astype(np.int64)
-
-    probe = rows_of(64)
-    t0 = time.perf_counter()
-    _, threads = oracle.attention_rows(pr, probe)
-    dt = time.perf_counter() - t0
-    n = int(max(64, min(case.B * case.Nq * case.S, 64 * target_s / max(dt, 1e-3))))
-    rows = rows_of(n)
-    t0 = time.perf_counter()
-    _, threads = oracle.attention_rows(pr, rows)
-    secs = time.perf_counter() - t0
-    if is_decode(idx):
-        es = torch.tensor([], dtype=case.dtype).element_size()
-        # bytes the sampled rows read from the KV cache (one kv row set per sampled row)
-        work = n * case.T * (case.H + case.Hv) * es
-        value, unit = work / secs / 1e9, "GB/s"
-    else:
-        work = float(counts[rows[:, 0], rows[:, 2]].sum()) * 2.0 * (case.H + case.Hv)
-        value, unit = work / secs / 1e12, "TFLOP/s"
-    return {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
-            "sample": f"{n} of {case.B * case.Nq * case.S} query rows of {case.name}, "
-                      f"{secs:.1f} s on {threads} threads", "seconds": secs}
+    """One timed oracle sample of about target_s seconds (the CPU-baseline leg)."""
+    return OracleSampler(idx, case).step(target_s)
 
 
 # ------------------------------------------------------------------------------ main
+
+def max_over_ranks(values, device="cpu"):
+    """Element-wise maximum of a list of floats over all ranks (identity without a group)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.cpu()]
+
 
 def dist_setup(backend):
     ws = int(os.environ.get("WORLD_SIZE", "1"))
@@ -317,7 +338,8 @@ def dist_setup(backend):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=3000,
+                    help="timed steps (the default keeps nvidia-smi sampling inside the timed region)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", type=int, default=2, choices=sorted(WORKLOADS))
@@ -325,6 +347,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0,
                     help="CPU work for the oracle baseline sample; 0 skips it")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the batch size of the headline workload (profiling captures only)")
+    ap.add_argument("--ref-seconds", type=float, default=150.0,
+                    help="total CPU time budget of the reference (oracle) arm")
     a = ap.parse_args()
     warmup = max(3, a.warmup)
     idx = a.workload
@@ -333,13 +359,14 @@ def main():
         ws, rank, _ = dist_setup("gloo")
         if rank != 0:
             return
-        case = workload(idx)
-        per_step = max(1.0, 150.0 / (a.steps + warmup))
+        sampler = OracleSampler(idx)
+        case = sampler.case
+        per_step = a.ref_seconds / (a.steps + warmup)
         for _ in range(warmup):
-            oracle_sample(idx, per_step / 4, case)
+            sampler.step(per_step)
         vals, secs, last = [], [], None
         for _ in range(a.steps):
-            last = oracle_sample(idx, per_step, case)
+            last = sampler.step(per_step)
             vals.append(last["value"])
             secs.append(last["seconds"])
         value = statistics.mean(vals)
@@ -369,15 +396,11 @@ def main():
         barrier()
     hbm, tfl, tfl_sus, src = peaks()
 
-    res = measure_native(idx, a.steps, warmup, barrier, with_e2e=not a.no_e2e)
+    res = measure_native(idx, a.steps, warmup, barrier, with_e2e=not a.no_e2e, batch=a.batch)
     case = res["case"]
     ms = statistics.mean(res["ms"])
     e2e_ms = statistics.mean(res["e2e_ms"]) if "e2e_ms" in res else float("nan")
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, e2e_ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], device="cuda")
     value, unit = metric_of(idx, case, ms)
     e2e_value, _ = metric_of(idx, case, e2e_ms)
     if rank != 0:
@@ -406,7 +429,7 @@ def main():
         for j in sorted(WORKLOADS):
             if j == idx:
                 continue
-            r = measure_native(j, max(5, a.steps // 2), warmup, barrier, with_e2e=False)
+            r = measure_native(j, max(5, min(a.steps // 2, 200)), warmup, barrier, with_e2e=False)
             m = statistics.mean(r["ms"])
             v, u = metric_of(j, r["case"], m)
             sec.append({"workload": r["case"].name, "value": v, "unit": u, "ms_per_step": m,

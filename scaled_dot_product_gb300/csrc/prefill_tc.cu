@@ -352,8 +352,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (ok) ok = load(&tv, j);
         }
       }
-      if (!ok) {
-        // let every copy already issued land before the CTA can exit
+      if (!ok || *abortp) {
+        // some role gave up: let every copy already issued land before the CTA can exit
         mbar_wait_bounded(b_q, 0, nullptr, kDrainNs);
         for (int s = 0; s < C::kStages && s < seq; ++s) {
           const int last = s + ((seq - 1 - s) / C::kStages) * C::kStages;

@@ -213,13 +213,16 @@ WORKLOADS = {
 }
 
 
-def workload(idx: int, small: bool = False, seed: Optional[int] = None) -> Case:
+def workload(idx: int, small: bool = False, seed: Optional[int] = None, batch: Optional[int] = None) -> Case:
+    """Named workload idx (1..5); `batch` overrides the batch size (for profiling captures
+    that must stay small)."""
     seed = 1000 + idx if seed is None else seed
     name = WORKLOADS[idx] + ("_small" if small else "")
     if idx == 1:
         return make_case(name, dtype=torch.float32, B=1, Nq=2, S=16, H=8, seed=seed)
     if idx == 2:
         B, S, Nq, Nkv, H = (2, 300, 8, 2, 128) if small else (2, 2048, 32, 8, 128)
+        B = batch if batch is not None else B
         return make_case(name, dtype=torch.bfloat16, B=B, Nq=Nq, Nkv=Nkv, S=S, H=H,
                          q_layout="bsnh", kv_layout="bsnh", seed=seed, causal="upper_left",
                          softcap=30.0, len_kind="nonpad", len_range=(S // 2, S))
@@ -233,6 +236,7 @@ def workload(idx: int, small: bool = False, seed: Optional[int] = None) -> Case:
         return c
     if idx == 4:
         B, N, P, H = (4, 4, 700, 128) if small else (64, 32, 4095, 128)
+        B = batch if batch is not None else B
         return make_case(name, dtype=torch.float16, B=B, Nq=N, S=1, L=1, P=P, H=H,
                          q_layout="bsnh", kv_layout="bsnh", seed=seed, want_present=True,
                          len_kind="keylen", len_range=((P + 1) // 4, P + 1))
