@@ -39,20 +39,25 @@ using namespace ptx;
 
 constexpr int kBM = 128;        // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;        // keys per tile
-#ifndef SDPA_TC_SPLIT
-#define SDPA_TC_SPLIT 1
-#endif
-constexpr int kSplit = SDPA_TC_SPLIT;             // softmax threads per query row (1 or 2)
-constexpr int kThreads = 128 + 256 * kSplit;      // 4 control warps + 2 tiles x kSplit warpgroups
+constexpr int kSplit = 1;                         // softmax threads per query row
 constexpr int kHalf = kBN / kSplit;               // score columns per softmax thread
-// Register split (setmaxnreg): the control warpgroup shrinks to kCtlRegs, the softmax
-// warpgroups grow to kSmxRegs.  The sum must not exceed what the block was launched with
-// (kThreads x the kernel's register count), which the host checks before every launch.
-constexpr int kLaunchRegs = (65536 / kThreads) & ~7;
-constexpr int kCtlRegs = 80;
-constexpr int kSmxRegs = ((kLaunchRegs * kThreads - kCtlRegs * 128) / (256 * kSplit)) & ~7;
-static_assert(kSmxRegs <= 256 && kSmxRegs >= kLaunchRegs, "register split");
-static_assert(kCtlRegs * 128 + kSmxRegs * 256 * kSplit <= kLaunchRegs * kThreads, "register split");
+
+// CTA shape for QT 128-row query tiles per CTA (1: two CTAs share an SM; 2: one CTA).
+template <int QT>
+struct Layout {
+  static constexpr int kQT = QT;
+  static constexpr int kSmxThreads = 128 * QT * kSplit;   // softmax warpgroups
+  static constexpr int kThreads = 128 + kSmxThreads;      // + 4 control warps
+  static constexpr int kMinBlocks = (QT == 1) ? 2 : 1;
+  // Register split (setmaxnreg): the control warpgroup shrinks to kCtlRegs, the softmax
+  // warpgroups grow to kSmxRegs.  The sum must not exceed what the block was launched with
+  // (kThreads x the kernel's register count), which the host checks before every launch.
+  static constexpr int kLaunchRegs = (65536 / (kThreads * kMinBlocks)) & ~7;
+  static constexpr int kCtlRegs = (QT == 1) ? 64 : 80;
+  static constexpr int kSmxRegs = ((kLaunchRegs * kThreads - kCtlRegs * 128) / kSmxThreads) & ~7;
+  static_assert(kSmxRegs <= 256 && kSmxRegs >= kLaunchRegs, "register split");
+  static_assert(kCtlRegs * 128 + kSmxRegs * kSmxThreads <= kLaunchRegs * kThreads, "register split");
+};
 constexpr float kRescaleThreshold = 8.f;   // log2 units
 // Softcap tanh(u) on |u| <= kTanhPolyLimit uses u - u^3/3 + 2u^5/15 on the FMA pipe: the
 // alternating Taylor series' error is below its next term, 17/315 u^7 <= 3.3e-6.
@@ -66,28 +71,30 @@ __device__ __forceinline__ float tanh_poly(float u) {
   return fmaf(w, q, u);
 }
 
-template <int H>
+template <int H, int kQT>
 struct Cfg {
   static constexpr int kRegions = H / 64;              // 128-byte swizzle regions per row
   static constexpr int kRegionBytes = 128 * 128;       // 128 rows x 128 bytes
   static constexpr int kQTile = kBM * H * 2;
   static constexpr int kKVTile = kBN * H * 2;
-  static constexpr int kStages = (H == 128) ? 4 : 10;
+  // ring depth: fill the shared memory one CTA (two tiles) or half of it (one tile) may use
+  static constexpr int kStages = (kQT == 2) ? ((H == 128) ? 4 : 10) : ((H == 128) ? 2 : 5);
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = 2 * kQTile;
+  static constexpr int kKVOff = kQT * kQTile;
   static constexpr int kSmem = kKVOff + kStages * kKVTile + 1024;   // + alignment slack
-  // Tensor memory (512 columns).  H = 128: S_A, S_B, O_A, O_B fill it, so P_X (16-bit,
-  // two per column) overwrites the first 64 columns of S_X once S_X is in registers.
-  // H = 64: P_A and P_B get columns of their own.
+  // Tensor memory: S_X (128 columns each), O_X (H columns each) and P_X (16-bit, two per
+  // column: 64 columns).  With H = 128 there is no room for P: P_X overwrites the first 64
+  // columns of S_X once S_X is in registers.
   static constexpr bool kAlias = (H == 128);
-  static constexpr int kTmemS0 = 0, kTmemS1 = 128, kTmemO0 = 256, kTmemO1 = 256 + H;
-  static constexpr int kTmemP0 = kAlias ? kTmemS0 : 256 + 2 * H;
-  static constexpr int kTmemP1 = kAlias ? kTmemS1 : 256 + 2 * H + 64;
-  static constexpr uint32_t kTmemCols = 512;
+  static constexpr int kTmemS0 = 0, kTmemS1 = 128;
+  static constexpr int kTmemO0 = 128 * kQT, kTmemO1 = kTmemO0 + H;
+  static constexpr int kTmemP0 = kAlias ? kTmemS0 : kTmemO0 + kQT * H;
+  static constexpr int kTmemP1 = kAlias ? kTmemS1 : kTmemP0 + 64;
+  static constexpr uint32_t kTmemCols = 256 * kQT;
 };
 
 struct TcArgs {
-  int B, Nq, Nkv, S, T, group, npairs;
+  int B, Nq, Nkv, S, T, group, nunits;
   float scale, scale_log2, cap_in, cap_out_log2;   // cap_* used when softcap > 0
   int has_softcap;
   int causal, window, len_kind;
@@ -234,21 +241,24 @@ __device__ __noinline__ float generic_score(const Rules& r, const RowCtx& ctx, f
 // Score-rule paths, fixed per launch.
 enum RuleMode { kPlain = 0, kAddMask = 1, kGeneric = 2 };
 
-template <int H, bool kBF16, int kMode>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int H, bool kBF16, int kMode, int QT>
+__global__ void __launch_bounds__(Layout<QT>::kThreads, Layout<QT>::kMinBlocks)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const TcArgs a) {
-  using C = Cfg<H>;
+  using C = Cfg<H, QT>;
+  using Lay = Layout<QT>;
+  constexpr int kQT = QT;
+  constexpr int kSmxThreads = Lay::kSmxThreads;
   using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_q, bar_qready, bar_drain;
   __shared__ __align__(8) uint64_t bar_full[C::kStages], bar_empty[C::kStages];
-  __shared__ __align__(8) uint64_t bar_sfull[2], bar_sfree[2], bar_pfull[2], bar_odone[2], bar_turn[2];
+  __shared__ __align__(8) uint64_t bar_sfull[2], bar_sfree[2], bar_pfull[2], bar_odone[2];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  __shared__ float red_max[2][2][kSplit][kBM];   // [tile parity][query tile][column part][row]
-  __shared__ float red_sum[2][kSplit][kBM];      // [query tile][column part][row]
+  __shared__ float red_max[2][kQT][kSplit][kSplit == 2 ? kBM : 1];   // [tile parity][query tile][part][row]
+  __shared__ float red_sum[kQT][kSplit][kSplit == 2 ? kBM : 1];      // [query tile][part][row]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -257,10 +267,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int g_idx = t % a.group; t /= a.group;
   const int kvh = t % a.Nkv; t /= a.Nkv;
   const int b = t % a.B; t /= a.B;
-  const int pair = a.npairs - 1 - t;
+  const int unit = a.nunits - 1 - t;
   const int qh = kvh * a.group + g_idx;
-  const int m0 = pair * 2 * kBM;
-  const int m1 = min(a.S, m0 + 2 * kBM);
+  const int m0 = unit * kQT * kBM;
+  const int m1 = min(a.S, m0 + kQT * kBM);
   const int64_t len_b = lens_of(a, b);
 
   // key tiles any row of this CTA can admit
@@ -281,22 +291,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto b_sfree = [&](int x) { return smem_u32(&bar_sfree[x]); };
   auto b_pfull = [&](int x) { return smem_u32(&bar_pfull[x]); };
   auto b_odone = [&](int x) { return smem_u32(&bar_odone[x]); };
-  auto b_turn = [&](int x) { return smem_u32(&bar_turn[x]); };
   volatile int* abortp = &abort_flag;
   constexpr uint64_t kDrainNs = 2000000000ull;
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     mbar_init(b_q, 1);
-    mbar_init(b_qready, 2 * kSplit * kBM);
+    mbar_init(b_qready, kSmxThreads);
     mbar_init(b_drain, 1);
     for (int s = 0; s < C::kStages; ++s) { mbar_init(b_full(s), 1); mbar_init(b_empty(s), 1); }
-    for (int x = 0; x < 2; ++x) {
+    for (int x = 0; x < kQT; ++x) {
       mbar_init(b_sfull(x), 1);
       mbar_init(b_sfree(x), kSplit * kBM);
       mbar_init(b_pfull(x), kSplit * kBM);
       mbar_init(b_odone(x), 1);
-      mbar_init(b_turn(x), kSplit * kBM);
     }
     fence_mbar_init();
   }
@@ -309,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_base_sh;
   // the control warpgroup hands registers to the softmax warpgroups
-  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtlRegs));
+  if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Lay::kCtlRegs));
 
   // Ring order of the K/V tiles follows their first use by the MMA warp.  With P aliasing S
   // (H = 128): K_0, V_0, K_1, V_1, ...  Otherwise S_X(j+1) is issued before PV_X(j), so the K
@@ -321,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
       int c1, c2, c3;
-      mbar_arrive_expect_tx(b_q, 2 * C::kQTile);
-      for (int x = 0; x < 2; ++x) {
+      mbar_arrive_expect_tx(b_q, kQT * C::kQTile);
+      for (int x = 0; x < kQT; ++x) {
         perm_coords(a.q_ds, a.q_dn, a.q_db, m0 + x * kBM, qh, b, c1, c2, c3);
         for (int r = 0; r < C::kRegions; ++r)
           tma_load_4d(sQ + x * C::kQTile + r * C::kRegionBytes, &tq, b_q, 64 * r, c1, c2, c3);
@@ -367,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0 && n_tiles > 0) {
       constexpr uint32_t kIdQK = idesc_f16(kBF16, kBM, kBN, false);
       constexpr uint32_t kIdPV = idesc_f16(kBF16, kBM, H, true);
-      const uint32_t tS[2] = {tmem + C::kTmemS0, tmem + C::kTmemS1};
+      const uint32_t tS[2] = {tmem + C::kTmemS0, tmem + C::kTmemS1};   // [1] unused with one tile
       const uint32_t tO[2] = {tmem + C::kTmemO0, tmem + C::kTmemO1};
       const uint32_t tP[2] = {tmem + C::kTmemP0, tmem + C::kTmemP1};
       int seq = 0;
@@ -399,10 +407,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok) ok = wait_full(seq);
       if (ok) {
         const int st = seq % C::kStages;
-        issue_S(0, st);
-        mma_commit(b_sfull(0));
-        issue_S(1, st);
-        mma_commit(b_sfull(1));
+        for (int x = 0; x < kQT; ++x) {
+          issue_S(x, st);
+          mma_commit(b_sfull(x));
+        }
         mma_commit(b_empty(st));
         ++seq;
       }
@@ -415,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!(ok = wait_full(seq))) break;
           ++seq;
           const int kst = seq % C::kStages;
-          for (int x = 0; x < 2 && ok; ++x) {
+          for (int x = 0; x < kQT && ok; ++x) {
             if (!(ok = mbar_wait_bounded(b_pfull(x), j & 1, abortp, a.wait_ns))) break;
             tc_fence_after();
             issue_PV(x, vst, j > 0);
@@ -439,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int kst = seq % C::kStages;
             if (!(ok = wait_full(seq))) break;
             ++seq;
-            for (int x = 0; x < 2 && ok; ++x) {
+            for (int x = 0; x < kQT && ok; ++x) {
               if (!(ok = mbar_wait_bounded(b_sfree(x), j & 1, abortp, a.wait_ns))) break;
               tc_fence_after();
               issue_S(x, kst);
@@ -451,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int vst = seq % C::kStages;
           if (!(ok = wait_full(seq))) break;
           ++seq;
-          for (int x = 0; x < 2 && ok; ++x) {
+          for (int x = 0; x < kQT && ok; ++x) {
             if (!(ok = mbar_wait_bounded(b_pfull(x), j & 1, abortp, a.wait_ns))) break;
             tc_fence_after();
             issue_PV(x, vst, j > 0);
@@ -470,7 +478,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ================================================================ softmax warpgroups
     // Four warpgroups: (query tile A or B) x (score columns 0-63 or 64-127).  The two
     // threads that share a row exchange their partial maxima through shared memory.
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSmxRegs));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Lay::kSmxRegs));
     const int g = (warp - 4) >> 2;
     const int x = g / kSplit;                       // query tile A or B
     const int hh = g % kSplit;                      // column part
@@ -558,15 +566,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(b_sfree(x));
       }
-      // Ping-pong: the two query tiles take turns through the exponent-heavy part, so that
-      // one works while the tensor core runs the other's products.  Tile A goes first.
-      if (x == 1 || j > 0) {
-        if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_turn(x), (x == 1 ? j : j - 1) & 1, abortp, a.wait_ns))))
-          break;
-      }
-      // keep the score arithmetic below the wait (it only touches registers)
-#pragma unroll
-      for (int e = 0; e < kHalf; ++e) asm volatile("" : "+f"(s[e]));
 
       const int key0 = (kv_t0 + j) * kBN + kHalf * hh;
       bool have_mx = false;       // set when the transform already produced this half's max
@@ -702,7 +701,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       f2_unpack(acc2[2], r4, r5);
       f2_unpack(acc2[3], r6, r7);
       l = l * corr + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
-      mbar_arrive_after(b_turn(x ^ 1), l);
 
       // PV_X(j-1) must be done: it reads P_X and accumulates into O_X (with P aliasing S,
       // the sfull_X completion already implied it)
@@ -855,33 +853,39 @@ uint64_t wait_limit_ns() {
   return v;
 }
 
-template <int H, bool kBF16, int kMode>
-cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TcArgs& a,
-                        int64_t units, cudaStream_t st) {
-  using C = Cfg<H>;
+template <int H, bool kBF16, int kMode, int QT>
+cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, TcArgs a,
+                        int64_t units_per_qt_row, cudaStream_t st) {
+  using C = Cfg<H, QT>;
+  using Lay = Layout<QT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, kBF16, kMode>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, kBF16, kMode, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     C::kSmem);
     // the in-kernel register split assumes the block is launched with kLaunchRegs per
     // thread; with fewer, the softmax warps' request could never be met
     cudaFuncAttributes fa{};
-    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<H, kBF16, kMode>);
-    if (attr_err == cudaSuccess && fa.numRegs < kLaunchRegs) attr_err = cudaErrorLaunchOutOfResources;
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<H, kBF16, kMode, QT>);
+    if (attr_err == cudaSuccess && fa.numRegs < Lay::kLaunchRegs) attr_err = cudaErrorLaunchOutOfResources;
   });
   if (attr_err != cudaSuccess) return attr_err;
-  prefill_tc_kernel<H, kBF16, kMode><<<(unsigned)units, kThreads, C::kSmem, st>>>(tq, tk, tv, a);
+  a.nunits = (a.S + QT * kBM - 1) / (QT * kBM);
+  const int64_t units = units_per_qt_row * a.nunits;
+  if (units > 0x7fffffff) return cudaErrorInvalidValue;
+  prefill_tc_kernel<H, kBF16, kMode, QT><<<(unsigned)units, Lay::kThreads, C::kSmem, st>>>(tq, tk, tv, a);
   count_launch(1);
   return cudaGetLastError();
 }
 
+// Plain rules run one 128-row tile per CTA (two CTAs per SM); the additive-mask and generic
+// paths, which need more registers per thread, run two tiles per CTA.
 template <int H, bool kBF16>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TcArgs& a,
-                     int64_t units, cudaStream_t st) {
-  if (a.generic) return launch_mode<H, kBF16, kGeneric>(tq, tk, tv, a, units, st);
-  if (a.add_fast) return launch_mode<H, kBF16, kAddMask>(tq, tk, tv, a, units, st);
-  return launch_mode<H, kBF16, kPlain>(tq, tk, tv, a, units, st);
+                     int64_t heads_batches, cudaStream_t st) {
+  if (a.generic) return launch_mode<H, kBF16, kGeneric, 2>(tq, tk, tv, a, heads_batches, st);
+  if (a.add_fast) return launch_mode<H, kBF16, kAddMask, 2>(tq, tk, tv, a, heads_batches, st);
+  return launch_mode<H, kBF16, kPlain, 1>(tq, tk, tv, a, heads_batches, st);
 }
 
 }  // namespace
@@ -899,7 +903,6 @@ bool tc_eligible(const Problem& p, sdpa_dtype dt) {
 cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, const char** name) {
   TcArgs a{};
   a.B = p.B; a.Nq = p.Nq; a.Nkv = p.Nkv; a.S = p.S; a.T = (int)p.T; a.group = p.group;
-  a.npairs = (p.S + 2 * kBM - 1) / (2 * kBM);
   a.scale = p.scale;
   a.scale_log2 = p.scale * kLog2e;
   a.has_softcap = p.r.softcap > 0.f;
@@ -911,7 +914,7 @@ cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, 
   a.lens = p.r.lens;
   const bool other_rules = (p.r.keep_kind != SDPA_KEEP_NONE) || (p.r.len_kind == SDPA_LEN_KEYLEN_I32);
   a.generic = other_rules;
-  a.add_fast = (p.r.add != nullptr) && !other_rules && p.r.add_dtype == (int)dt && kSplit == 1;
+  a.add_fast = (p.r.add != nullptr) && !other_rules && p.r.add_dtype == (int)dt;
   if (p.r.add != nullptr && !a.add_fast) a.generic = 1;
   if (a.add_fast) {
     // widest load every mask row start allows (key offsets are multiples of 32 elements)
@@ -935,8 +938,7 @@ cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, 
   int vds, vdn, vdb;
   if (!make_map(&tv, p.v, dt, p.B, p.Nkv, p.T, p.Hv, &vds, &vdn, &vdb)) return cudaErrorInvalidValue;
   if (vds != a.kv_ds || vdn != a.kv_dn || vdb != a.kv_db) return cudaErrorInvalidValue;   // k and v views differ in order
-  const int64_t units = (int64_t)p.B * p.Nkv * a.npairs * p.group;
-  if (units > 0x7fffffff) return cudaErrorInvalidValue;
+  const int64_t units = (int64_t)p.B * p.Nkv * p.group;   // times the query units, per layout
   const bool bf = dt == SDPA_BF16;
   if (p.H == 128) {
     *name = bf ? "prefill_tc_bf16_h128" : "prefill_tc_f16_h128";
