@@ -84,6 +84,10 @@ def lib():
         _lib.oracle_present.restype = ctypes.c_int
         _lib.oracle_present.argtypes = [ctypes.c_int32] * 6 + [ctypes.POINTER(_Tensor)] * 2 + \
             [ctypes.c_void_p, ctypes.c_void_p]
+        _lib.oracle_rotary.restype = ctypes.c_int
+        _lib.oracle_rotary.argtypes = [ctypes.c_int32] * 4 + [ctypes.POINTER(_Tensor), ctypes.c_int32,
+                                       ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int32,
+                                       ctypes.c_int64, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
         _lib.oracle_to_double.restype = ctypes.c_double
         _lib.oracle_to_double.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64]
         _lib.oracle_round_f16.restype = ctypes.c_uint16
@@ -225,3 +229,30 @@ def round_f16(x: float) -> int:
 
 def round_bf16(x: float) -> int:
     return int(lib().oracle_round_bf16(float(x)))
+
+
+def rotary(x: torch.Tensor, cos_cache: torch.Tensor, sin_cache: torch.Tensor,
+           position_ids: Optional[torch.Tensor] = None, rotary_dim: int = 0,
+           interleaved: bool = False) -> np.ndarray:
+    """RotaryEmbedding of a (B, N, S, D) CPU view; returns float64 (B, N, S, D).
+
+    cos_cache / sin_cache: rank-2 (max_pos, R/2) with position_ids (B, S) int64, or rank-3
+    (B, S, R/2) without position ids."""
+    B, N, S, D = x.shape
+    keep: list = []
+    xv = _view(x, keep)
+    cc, sc = cos_cache.contiguous(), sin_cache.contiguous()
+    keep += [cc, sc]
+    ld = cc.shape[-1]
+    pos_ptr, pos_sb = None, 0
+    if position_ids is not None:
+        pid = position_ids.to(torch.int64).contiguous()
+        keep.append(pid)
+        pos_ptr, pos_sb = pid.data_ptr(), pid.shape[-1] if pid.dim() == 2 else 0
+    out = np.zeros((B, N, S, D), dtype=np.float64)
+    rc = lib().oracle_rotary(B, N, S, D, ctypes.byref(xv), int(rotary_dim), int(bool(interleaved)),
+                             cc.data_ptr(), sc.data_ptr(), _DT[cc.dtype], ld, pos_ptr, pos_sb,
+                             out.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_rotary rejected its arguments")
+    return out

@@ -327,3 +327,33 @@ int oracle_present(int32_t dtype, int32_t B, int32_t N, int32_t P, int32_t L, in
       }
   return 0;
 }
+
+/* ---- rotary positional embedding (class RotaryEmbedding; RoFormer's rotation of channel
+ * pairs by position-dependent angles given through the cos / sin caches) ---- */
+
+int oracle_rotary(int32_t B, int32_t N, int32_t S, int32_t D, const orc_tensor* x, int32_t rotary_dim,
+                  int32_t interleaved, const void* cos_cache, const void* sin_cache, int32_t cache_dtype,
+                  int64_t cache_ld, const int64_t* positions, int64_t pos_sb, double* out) {
+  const int32_t R = rotary_dim > 0 ? rotary_dim : D;
+  if (R > D || R % 2 != 0 || !x || !cos_cache || !sin_cache) return -1;
+  const int32_t half = R / 2;
+  for (int64_t b = 0; b < B; ++b)
+    for (int64_t n = 0; n < N; ++n)
+      for (int64_t s = 0; s < S; ++s) {
+        const int64_t xo = offset4(x, b, n, s);
+        double* o = out + ((b * N + n) * S + s) * D;
+        for (int64_t d = 0; d < D; ++d) o[d] = oracle_to_double(x->dtype, x->data, xo + d);
+        const int64_t row = positions ? positions[b * pos_sb + s] : b * S + s;
+        for (int64_t d = 0; d < half; ++d) {
+          const double c = oracle_to_double(cache_dtype, cos_cache, row * cache_ld + d);
+          const double sn = oracle_to_double(cache_dtype, sin_cache, row * cache_ld + d);
+          const int64_t i1 = interleaved ? 2 * d : d;
+          const int64_t i2 = interleaved ? 2 * d + 1 : d + half;
+          const double x1 = oracle_to_double(x->dtype, x->data, xo + i1);
+          const double x2 = oracle_to_double(x->dtype, x->data, xo + i2);
+          o[i1] = x1 * c - x2 * sn;
+          o[i2] = x2 * c + x1 * sn;
+        }
+      }
+  return 0;
+}

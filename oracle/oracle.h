@@ -87,6 +87,17 @@ int oracle_attention_rows(const orc_params* p, const int64_t* rows, int64_t nrow
 int oracle_present(int32_t dtype, int32_t B, int32_t N, int32_t P, int32_t L, int32_t D,
                    const orc_tensor* past, const orc_tensor* cur, const void* bias, void* out);
 
+/* Rotary positional embedding (onnx-light "include_nn_kernels.h", class RotaryEmbedding):
+ * x is a (B, N, S, D) view; out is a contiguous (B, N, S, D) double array.  Channel pairs
+ * are (d, d + R/2) for d < R/2, or (2d, 2d + 1) when interleaved; R = rotary_dim (0 means
+ * D).  Each pair (x1, x2) becomes (x1 cos - x2 sin, x2 cos + x1 sin) with cos = cos[pos, d]
+ * and sin = sin[pos, d]; channels >= R pass through.  The angle row comes from
+ * positions[b * pos_sb + s] (int64) indexing a rank-2 cache (row stride cache_ld), or,
+ * when positions is NULL, from the rank-3 cache row (b * S + s). */
+int oracle_rotary(int32_t B, int32_t N, int32_t S, int32_t D, const orc_tensor* x, int32_t rotary_dim,
+                  int32_t interleaved, const void* cos_cache, const void* sin_cache, int32_t cache_dtype,
+                  int64_t cache_ld, const int64_t* positions, int64_t pos_sb, double* out);
+
 /* Element conversions, exposed so they can be pinned against library conversions. */
 double oracle_to_double(int32_t dtype, const void* base, int64_t index);
 uint16_t oracle_round_f16(double x);

@@ -25,6 +25,9 @@ MUTATIONS = {
     "f16_exponent_bias": ("e - 25);", "e - 24);"),
     "past_not_first": ("if (j < p->P) {", "if (j >= p->L) {"),
     "kv_bias_on_values_uses_key_width": ("kh * D + d)", "kh * p->H + d)"),
+    "rotary_sign": ("o[i1] = x1 * c - x2 * sn;", "o[i1] = x1 * c + x2 * sn;"),
+    "rotary_pairs_adjacent_always": ("const int64_t i2 = interleaved ? 2 * d + 1 : d + half;",
+                                     "const int64_t i2 = 2 * d + 1;"),
 }
 
 

@@ -410,3 +410,85 @@ def test_oracle_rejects_window_without_causal_and_bad_groups():
     q2 = rnd(1, 2, 2, 4, seed=78)
     with pytest.raises(ValueError):
         run(q2, k, v, window=2)
+
+
+# ---------------------------------------------------------------- rotary embedding (class RotaryEmbedding)
+
+def _rope_caches(max_pos, half, base=10000.0, dtype=torch.float64):
+    """cos/sin tables of RoFormer's angles pos * base^(-2d/R) (test input, not the oracle)."""
+    pos = torch.arange(max_pos, dtype=torch.float64).view(-1, 1)
+    inv = base ** (-torch.arange(half, dtype=torch.float64) * 2.0 / (2 * half))
+    ang = pos * inv.view(1, -1)
+    return torch.cos(ang).to(dtype), torch.sin(ang).to(dtype)
+
+
+def test_rotary_identity_and_quarter_turn():
+    B, N, S, D = 2, 3, 4, 8
+    x = rnd(B, N, S, D, seed=80)
+    one, zero = torch.ones(5, D // 2, dtype=torch.float64), torch.zeros(5, D // 2, dtype=torch.float64)
+    pid = torch.tensor([[0, 1, 2, 3], [4, 3, 2, 1]], dtype=torch.int64)
+    for inter in (False, True):
+        np.testing.assert_array_equal(oracle.rotary(x, one, zero, pid, interleaved=inter), x.numpy())
+        got = oracle.rotary(x, zero, one, pid, interleaved=inter)       # 90 degrees
+        xn = x.numpy()
+        if inter:
+            x1, x2, g1, g2 = xn[..., 0::2], xn[..., 1::2], got[..., 0::2], got[..., 1::2]
+        else:
+            x1, x2, g1, g2 = xn[..., :D // 2], xn[..., D // 2:], got[..., :D // 2], got[..., D // 2:]
+        np.testing.assert_array_equal(g1, -x2)
+        np.testing.assert_array_equal(g2, x1)
+
+
+def test_rotary_equals_complex_multiplication():
+    B, N, S, D = 1, 2, 6, 16
+    x = rnd(B, N, S, D, seed=81)
+    cos, sin = _rope_caches(32, D // 2)
+    pid = torch.tensor([[5, 0, 31, 7, 7, 12]], dtype=torch.int64)
+    got = oracle.rotary(x, cos, sin, pid)
+    xn = x.numpy()
+    z = (xn[..., :D // 2] + 1j * xn[..., D // 2:]) * np.exp(1j * np.angle(cos.numpy() + 1j * sin.numpy()))[pid.numpy()[0]]
+    np.testing.assert_allclose(got[..., :D // 2], z.real, atol=1e-12)
+    np.testing.assert_allclose(got[..., D // 2:], z.imag, atol=1e-12)
+
+
+def test_rotary_scores_depend_only_on_relative_position():
+    D = 32
+    q, k = rnd(1, 1, 1, D, seed=82), rnd(1, 1, 1, D, seed=83)
+    cos, sin = _rope_caches(64, D // 2)
+    def score(pq, pk):
+        rq = oracle.rotary(q, cos, sin, torch.tensor([[pq]]))
+        rk = oracle.rotary(k, cos, sin, torch.tensor([[pk]]))
+        return float((rq * rk).sum())
+    base = score(9, 4)
+    for shift in (1, 7, 40):
+        assert score(9 + shift, 4 + shift) == pytest.approx(base, abs=1e-10)
+    assert abs(score(9, 4) - score(9, 5)) > 1e-6
+
+
+def test_rotary_interleaved_is_a_channel_permutation_of_the_half_layout():
+    B, N, S, D = 2, 2, 3, 12
+    x = rnd(B, N, S, D, seed=84)
+    cos, sin = _rope_caches(8, D // 2)
+    pid = torch.tensor([[1, 2, 3], [7, 0, 5]], dtype=torch.int64)
+    perm = np.concatenate([np.arange(0, D, 2), np.arange(1, D, 2)])    # interleaved -> halves
+    inter = oracle.rotary(x, cos, sin, pid, interleaved=True)
+    half = oracle.rotary(x[..., perm].contiguous(), cos, sin, pid)
+    np.testing.assert_allclose(inter[..., perm], half, atol=1e-14)
+
+
+def test_rotary_partial_dim_passes_the_rest_and_caches_forms_agree():
+    B, N, S, D, R = 2, 2, 4, 16, 8
+    x = rnd(B, N, S, D, seed=85)
+    cos, sin = _rope_caches(10, R // 2)
+    pid = torch.tensor([[0, 3, 9, 2], [1, 1, 4, 8]], dtype=torch.int64)
+    got = oracle.rotary(x, cos, sin, pid, rotary_dim=R)
+    np.testing.assert_array_equal(got[..., R:], x.numpy()[..., R:])
+    sub = oracle.rotary(x[..., :R].contiguous(), cos, sin, pid)
+    np.testing.assert_allclose(got[..., :R], sub, atol=1e-14)
+    # rank-3 caches (B, S, R/2) used directly equal rank-2 caches gathered by position ids
+    cos3, sin3 = cos[pid], sin[pid]
+    np.testing.assert_array_equal(oracle.rotary(x, cos3, sin3, None, rotary_dim=R), got)
+    # every rotated pair keeps its length
+    n_in = x.numpy()[..., :R // 2] ** 2 + x.numpy()[..., R // 2:R] ** 2
+    n_out = got[..., :R // 2] ** 2 + got[..., R // 2:R] ** 2
+    np.testing.assert_allclose(n_out, n_in, rtol=1e-12)
