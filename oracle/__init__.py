@@ -94,6 +94,8 @@ def lib():
         _lib.oracle_round_f16.argtypes = [ctypes.c_double]
         _lib.oracle_round_bf16.restype = ctypes.c_uint16
         _lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        _lib.oracle_round_array.restype = ctypes.c_int
+        _lib.oracle_round_array.argtypes = [ctypes.c_int32, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p]
     return _lib
 
 
@@ -229,6 +231,28 @@ def round_f16(x: float) -> int:
 
 def round_bf16(x: float) -> int:
     return int(lib().oracle_round_bf16(float(x)))
+
+
+def round_array(x: np.ndarray, dtype: torch.dtype) -> torch.Tensor:
+    """Rounds a float64 array once, to nearest even, to dtype (the oracle's own rounding)."""
+    a = np.ascontiguousarray(x, dtype=np.float64)
+    out = torch.empty(a.shape, dtype=dtype)
+    if lib().oracle_round_array(_DT[dtype], a.ctypes.data, a.size, out.data_ptr()) != 0:
+        raise ValueError("oracle_round_array: dtype must be float32, float16 or bfloat16")
+    return out
+
+
+def gqa_rotary_positions(B: int, S: int, L: int, T: int, seqlens_k: Optional[torch.Tensor] = None):
+    """Absolute positions of the rotated rows ("Microsoft GroupQueryAttention": RoPE uses
+    absolute positions).  The S query rows and the L new key rows are the last rows of
+    the valid sequence of Tv(b) keys, Tv(b) = seqlens_k[b] + 1 when given, else T: query
+    i at Tv(b) - S + i, new key j at Tv(b) - L + j (the causal alignment's positions).
+    Returns (B, S) and (B, L) int64 tensors."""
+    if seqlens_k is not None:
+        tv = seqlens_k.to(torch.int64).view(B, 1) + 1
+    else:
+        tv = torch.full((B, 1), T, dtype=torch.int64)
+    return tv - S + torch.arange(S).view(1, S), tv - L + torch.arange(L).view(1, L)
 
 
 def rotary(x: torch.Tensor, cos_cache: torch.Tensor, sin_cache: torch.Tensor,

@@ -297,6 +297,18 @@ int oracle_attention_rows(const orc_params* p, const int64_t* rows, int64_t nrow
   return status ? status : nthreads;
 }
 
+/* ---- rounding of a double array to an element type (once, to nearest even) ---- */
+
+int oracle_round_array(int32_t dtype, const double* in, int64_t n, void* out) {
+  if (dtype != ORC_F32 && dtype != ORC_F16 && dtype != ORC_BF16) return -1;
+  for (int64_t i = 0; i < n; ++i) {
+    if (dtype == ORC_F32) ((float*)out)[i] = (float)in[i];
+    else if (dtype == ORC_F16) ((uint16_t*)out)[i] = oracle_round_f16(in[i]);
+    else ((uint16_t*)out)[i] = oracle_round_bf16(in[i]);
+  }
+  return 0;
+}
+
 /* ---- present = concat(past, new) along the sequence axis ---- */
 
 int oracle_present(int32_t dtype, int32_t B, int32_t N, int32_t P, int32_t L, int32_t D,

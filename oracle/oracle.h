@@ -102,6 +102,8 @@ int oracle_rotary(int32_t B, int32_t N, int32_t S, int32_t D, const orc_tensor* 
 double oracle_to_double(int32_t dtype, const void* base, int64_t index);
 uint16_t oracle_round_f16(double x);
 uint16_t oracle_round_bf16(double x);
+/* n doubles rounded once to dtype (F32 / F16 / BF16), written contiguously to out. */
+int oracle_round_array(int32_t dtype, const double* in, int64_t n, void* out);
 
 #ifdef __cplusplus
 }

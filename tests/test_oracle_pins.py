@@ -88,6 +88,25 @@ def test_bf16_rounding_matches_torch():
     assert bad.size == 0, [(float(xs[i]), hex(got[i]), hex(want[i])) for i in bad[:5]]
 
 
+def test_array_rounding_is_one_rounding_from_double():
+    """round_array rounds doubles once: it matches numpy's direct double->half conversion
+    and the scalar (pinned) roundings, and does not round through float32 first."""
+    rng = np.random.default_rng(7)
+    xs = np.concatenate([rng.standard_normal(4000) * 10.0 ** rng.integers(-6, 5, 4000),
+                         _rounding_samples().astype(np.float64)])
+    with np.errstate(over="ignore"):
+        np.testing.assert_array_equal(oracle.round_array(xs, torch.float16).view(torch.int16).numpy(),
+                                      xs.astype(np.float16).view(np.int16))
+    got = oracle.round_array(xs, torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(got, np.array([oracle.round_bf16(x) for x in xs], dtype=np.uint16))
+    np.testing.assert_array_equal(oracle.round_array(xs, torch.float32).numpy(), xs.astype(np.float32))
+    # just above a bf16 tie by less than a float32 ulp: a float32 detour would round to even (down)
+    x = 1.0 + 2.0 ** -8 + 2.0 ** -40
+    assert float(oracle.round_array(np.array([x]), torch.bfloat16)[0]) == 1.0 + 2.0 ** -7
+    x = 1.0 + 2.0 ** -11 + 2.0 ** -40                     # same for float16
+    assert float(oracle.round_array(np.array([x]), torch.float16)[0]) == 1.0 + 2.0 ** -10
+
+
 # ---------------------------------------------------------------- library special cases
 
 @pytest.mark.parametrize("shape", [(1, 2, 16, 16, 8), (2, 3, 5, 9, 16), (1, 1, 1, 7, 4)])
@@ -492,3 +511,17 @@ def test_rotary_partial_dim_passes_the_rest_and_caches_forms_agree():
     n_in = x.numpy()[..., :R // 2] ** 2 + x.numpy()[..., R // 2:R] ** 2
     n_out = got[..., :R // 2] ** 2 + got[..., R // 2:R] ** 2
     np.testing.assert_allclose(n_out, n_in, rtol=1e-12)
+
+
+def test_gqa_rotary_positions():
+    """Absolute positions: a prompt without past starts at 0, a decode step after P past
+    rows sits at P, seqlens_k moves the end of the valid sequence, and the query and new
+    key rows end together at Tv - 1."""
+    qp, kp = oracle.gqa_rotary_positions(1, 4, 4, 4)
+    assert qp.tolist() == [[0, 1, 2, 3]] and kp.tolist() == [[0, 1, 2, 3]]
+    qp, kp = oracle.gqa_rotary_positions(2, 1, 1, 11)
+    assert qp.tolist() == [[10], [10]] and kp.tolist() == [[10], [10]]
+    qp, kp = oracle.gqa_rotary_positions(2, 1, 1, 11, torch.tensor([5, 9], dtype=torch.int32))
+    assert qp.tolist() == [[5], [9]] and kp.tolist() == [[5], [9]]
+    qp, kp = oracle.gqa_rotary_positions(1, 3, 4, 10)
+    assert qp.tolist() == [[7, 8, 9]] and kp.tolist() == [[6, 7, 8, 9]]
