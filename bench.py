@@ -193,9 +193,21 @@ def time_device(fn, steps, warmup, flush_buf, barrier):
     return ms, wall
 
 
-def measure_native(idx: int, steps: int, warmup: int, barrier, with_e2e: bool = True, batch=None):
+def with_rope(case: Case) -> Case:
+    """The same case with GroupQueryAttention's rotary step on Q and the new K rows
+    (rank-2 cos/sin tables of T rows over all H channels)."""
+    from scaled_dot_product_gb300.workloads import rope_caches
+    case.rotary_cos, case.rotary_sin = rope_caches(case.T, case.H // 2, case.dtype)
+    case.name += "_rope"
+    return case
+
+
+def measure_native(idx: int, steps: int, warmup: int, barrier, with_e2e: bool = True, batch=None,
+                   rope: bool = False):
     from scaled_dot_product_gb300 import sdpa
     case_cpu = workload(idx, batch=batch)
+    if rope:
+        case_cpu = with_rope(case_cpu)
     case = case_cpu.to("cuda")
     op = "decode" if is_decode(idx) else "fwd"
     ws = sdpa.case_workspace(case, op)
@@ -242,6 +254,38 @@ def measure_native(idx: int, steps: int, warmup: int, barrier, with_e2e: bool = 
         e_ms, _ = time_device(e2e_step, e_steps, 2, None, barrier)
         res.update(e2e_ms=e_ms, h2d=h2d, d2h=d2h)
     return res
+
+
+ROTARY_SHAPE = dict(B=4, N=32, S=4096, D=128)     # packed (B, S, N*D) bf16, 128 MiB in and out
+
+
+def rotary_bytes(B, N, S, D, esize, R=None):
+    """Algorithmic bytes of one standalone rotary call: x read, y written, one int64
+    position id and one cos and one sin row (R/2 entries) per (b, s)."""
+    R = D if R is None else R
+    return 2 * B * N * S * D * esize + B * S * 8 + 2 * B * S * (R // 2) * esize
+
+
+def measure_rotary(steps: int, warmup: int, barrier, hbm: float):
+    from scaled_dot_product_gb300 import sdpa
+    from scaled_dot_product_gb300.workloads import make_rotary_inputs
+    sh = ROTARY_SHAPE
+    ri = make_rotary_inputs(dtype=torch.bfloat16, layout="bsnh", cache="ids", max_pos=2 * sh["S"],
+                            seed=7, **sh).to("cuda")
+    y = torch.empty_like(ri.x)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    run = lambda: sdpa.sdpa_rotary(ri.x, ri.cos, ri.sin, ri.position_ids, num_heads=sh["N"], y=y)
+    run()
+    torch.cuda.synchronize()
+    n0 = sdpa.sdpa_launch_count()
+    ms, _ = time_device(run, steps, warmup, flush, barrier)
+    launches = sdpa.sdpa_launch_count() - n0
+    m = statistics.mean(ms)
+    gbs = rotary_bytes(sh["B"], sh["N"], sh["S"], sh["D"], 2) / (m * 1e-3) / 1e9
+    return {"workload": "rotary_bf16_b4_s4096_n32_d128_position_ids", "value": gbs, "unit": "GB/s",
+            "ms_per_step": m, "kernel": "rotary", "gpu_launches": launches,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                         "traffic": None}, "l2_flush": True}
 
 
 def metric_of(idx: int, case: Case, ms: float):
@@ -439,6 +483,22 @@ def main():
             del r
             torch.cuda.empty_cache()
         line["secondary"] = sec
+        # the rotary embedding: standalone, and as the prologue of the GQA prefill and of
+        # the decode step (overhead against the same workload without it)
+        nxt = [measure_rotary(max(20, min(a.steps, 500)), warmup, barrier, hbm)]
+        for j in (2, 4):
+            r = measure_native(j, max(5, min(a.steps // 2, 200)), warmup, barrier, with_e2e=False, rope=True)
+            m = statistics.mean(r["ms"])
+            v, u = metric_of(j, r["case"], m)
+            base_ms = ms if j == idx else next((x["ms_per_step"] for x in sec if x["workload"] ==
+                                               WORKLOADS[j]), None)
+            nxt.append({"workload": r["case"].name, "value": v, "unit": u, "ms_per_step": m,
+                        "kernel": r["kernel"], "gpu_launches": r["launches"],
+                        "rope_overhead_ms": None if base_ms is None else m - base_ms,
+                        "l2_flush": r["l2_flush"], "clocks": r["clocks"]})
+            del r
+            torch.cuda.empty_cache()
+        line["rotary"] = nxt
     print(json.dumps(line))
 
 

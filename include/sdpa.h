@@ -145,6 +145,17 @@ typedef struct {
   const void* lens;             /* (B) device vector                                         */
   float mask_filter_value;      /* MHA: -10000                                               */
   int32_t softcap_before_bias;  /* 0: pages' stage order; 1: softcap, then the additive mask */
+  /* Rotary embedding of Q and of the new K rows before attention (GroupQueryAttention's
+   * rotary, class RotaryEmbedding's rotation): rank-2 caches (rotary_max_pos, R/2) in
+   * dtype, R = rotary_dim (0: H).  Absolute positions: query row i at Tv(b) - S + i and new
+   * key row j at Tv(b) - L + j, Tv(b) = seqlens_k[b] + 1 under SDPA_LEN_SEQLENS_K_I32, else
+   * T = P + L.  present holds the rotated keys.  A position outside the cache is reported
+   * by sdpa_query_status as SDPA_ERR_INVALID.  rotary_cos == NULL: no rotation. */
+  const void* rotary_cos;
+  const void* rotary_sin;
+  int64_t rotary_max_pos;
+  int32_t rotary_dim;
+  int32_t rotary_interleaved;
 } sdpa_params;
 
 /* Which entry point a workspace query is for. */
@@ -199,6 +210,20 @@ SDPA_API size_t sdpa_workspace_size(const sdpa_params* p, int op);
  * launch.  No CUDA call.  Returns SDPA_OK or the error code the entry point would return. */
 SDPA_API int sdpa_validate(const sdpa_params* p, int op);
 
+/* RotaryEmbedding (onnx-light "include_nn_kernels.h", class RotaryEmbedding): y = x with
+ * the first R channels of every head rotated in pairs (d, d + R/2), or (2d, 2d + 1) when
+ * interleaved, by the angle of cache row `pos`: (x1, x2) -> (x1 cos - x2 sin, x2 cos + x1 sin);
+ * channels >= R are copied.  x, y: (B, N, S, D) views (rank-3 or rank-4 via strides), dtype
+ * elements, may not overlap.  Caches: R/2 contiguous entries per row in dtype; with
+ * position_ids (B, S) int64 (device) they are rank-2 (max_pos rows) and row = position_ids[b,
+ * s]; with position_ids NULL they are rank-3 (B, S, R/2) and max_pos must be B*S.
+ * R = rotary_dim (0: D), even.  Positions outside [0, max_pos) are reported by
+ * sdpa_query_status as SDPA_ERR_INVALID. */
+SDPA_API int sdpa_rotary(sdpa_dtype dtype, int32_t B, int32_t N, int32_t S, int32_t D, sdpa_view x, sdpa_view y,
+                         const void* cos_cache, const void* sin_cache, int64_t max_pos,
+                         const int64_t* position_ids, int32_t rotary_dim, int32_t interleaved,
+                         sdpa_stream_t stream);
+
 /* present[b, n, 0:P] = past[b, n, :]; present[b, n, P:P+L] = cur[b, n, :] (+ bias[n*D:(n+1)*D]
  * rounded once to dtype when bias is non-NULL).  (class Attention, past_key/past_value
  * and Result.present_key; MHA: present holds P+L positions; GQA: present holds the whole
@@ -209,9 +234,10 @@ SDPA_API int sdpa_kv_concat(sdpa_dtype dtype, int32_t B, int32_t N, int32_t P, i
                    sdpa_view past, sdpa_view cur, const void* bias, sdpa_view present,
                    sdpa_stream_t stream);
 
-/* Synchronises `stream`, then reads and clears the current device's status word, which a
- * kernel sets when one of its bounded waits expires.  Returns SDPA_OK, SDPA_ERR_TIMEOUT,
- * or SDPA_ERR_CUDA when the synchronisation itself failed. */
+/* Synchronises `stream`, then reads and clears the current device's status words: set when
+ * a bounded wait of a kernel expires (SDPA_ERR_TIMEOUT) or a rotary position falls outside
+ * its cache (SDPA_ERR_INVALID).  Returns SDPA_OK, one of those codes, or SDPA_ERR_CUDA when
+ * the synchronisation itself failed. */
 SDPA_API int sdpa_query_status(sdpa_stream_t stream);
 
 /* Message for the last error on the calling thread ("" when none).  Valid until the next

@@ -91,8 +91,17 @@ Extent flat(const void* p, size_t bytes, const char* name) {
   return e;
 }
 
-// Validation shared by every attention entry point.  Fills `pr` on success.
-int validate(const sdpa_params* p, int op, Problem* pr) {
+// Rotary embedding of Q and the new K rows requested through sdpa_params.
+struct Rot {
+  bool on = false;
+  const void* cos = nullptr;
+  const void* sin = nullptr;
+  int64_t max_pos = 0;
+  int R = 0, interleaved = 0;
+};
+
+// Validation shared by every attention entry point.  Fills `pr` (and `rot`) on success.
+int validate(const sdpa_params* p, int op, Problem* pr, Rot* rot = nullptr) {
   if (!p) return fail(SDPA_ERR_NULL, "params is NULL");
   if (p->struct_size != (int32_t)sizeof(sdpa_params))
     return fail(SDPA_ERR_INVALID, "struct_size %d != sizeof(sdpa_params) %d", p->struct_size,
@@ -135,6 +144,22 @@ int validate(const sdpa_params* p, int op, Problem* pr) {
     return fail(SDPA_ERR_SHAPE, "P=%d past rows but past_k/past_v absent", p->P);
   if (p->P == 0 && (p->past_k.data || p->past_v.data))
     return fail(SDPA_ERR_SHAPE, "past_k/past_v given with P=0");
+  if ((p->rotary_cos == nullptr) != (p->rotary_sin == nullptr))
+    return fail(SDPA_ERR_INVALID, "rotary_cos and rotary_sin must be given together");
+  const bool rot_on = p->rotary_cos != nullptr;
+  const int rot_R = rot_on ? (p->rotary_dim ? p->rotary_dim : p->H) : 0;
+  if (rot_on) {
+    if (rot_R < 2 || rot_R > p->H || rot_R % 2)
+      return fail(SDPA_ERR_INVALID, "rotary_dim %d: must be even and in [2, H=%d] (0 means H)", p->rotary_dim, p->H);
+    if (p->rotary_interleaved != 0 && p->rotary_interleaved != 1)
+      return fail(SDPA_ERR_INVALID, "rotary_interleaved must be 0 or 1");
+    if (p->rotary_max_pos < 1 || p->rotary_max_pos > ((int64_t)1 << 40))
+      return fail(SDPA_ERR_SHAPE, "rotary_max_pos %lld out of range", (long long)p->rotary_max_pos);
+    if (p->q_bias || p->k_bias)
+      return fail(SDPA_ERR_UNSUPPORTED, "rotary embedding together with q/k projection biases");
+    if (((uintptr_t)p->rotary_cos | (uintptr_t)p->rotary_sin) % esize(dt))
+      return fail(SDPA_ERR_ALIGNMENT, "rotary caches not aligned to the element size");
+  }
   if (op == SDPA_OP_DECODE) {
     if (p->S > 16) return fail(SDPA_ERR_UNSUPPORTED, "decode handles S <= 16 (S=%d); use sdpa_attn_fwd", p->S);
     if (!decode_supported((sdpa_dtype)dt, p->H, p->Hv))
@@ -179,7 +204,9 @@ int validate(const sdpa_params* p, int op, Problem* pr) {
                            flat(p->k_bias, (size_t)p->Nkv * p->H * esize(dt), "k_bias"),
                            flat(p->v_bias, (size_t)p->Nkv * p->Hv * esize(dt), "v_bias"),
                            flat(p->head_sink, (size_t)p->Nq * esize(dt), "head_sink"),
-                           flat(p->lens, (size_t)p->B * (p->len_kind == SDPA_LEN_NONPAD_I64 ? 8 : 4), "lens")};
+                           flat(p->lens, (size_t)p->B * (p->len_kind == SDPA_LEN_NONPAD_I64 ? 8 : 4), "lens"),
+                           flat(p->rotary_cos, (size_t)p->rotary_max_pos * (rot_R / 2) * esize(dt), "rotary_cos"),
+                           flat(p->rotary_sin, (size_t)p->rotary_max_pos * (rot_R / 2) * esize(dt), "rotary_sin")};
   for (const Extent& o : {ey, eprk, eprv}) {
     for (const Extent& in : inputs)
       if (overlap(o, in)) return fail(SDPA_ERR_ALIAS, "output %s overlaps input %s", o.name, in.name);
@@ -211,6 +238,13 @@ int validate(const sdpa_params* p, int op, Problem* pr) {
   ru.softcap = p->softcap > 0.f ? p->softcap : 0.f;
   ru.softcap_before_bias = p->softcap_before_bias ? 1 : 0;
   ru.filter = p->mask_filter_value;
+  if (rot) {
+    *rot = Rot{};
+    if (rot_on) {
+      rot->on = true; rot->cos = p->rotary_cos; rot->sin = p->rotary_sin;
+      rot->max_pos = p->rotary_max_pos; rot->R = rot_R; rot->interleaved = p->rotary_interleaved;
+    }
+  }
   return SDPA_OK;
 }
 
@@ -220,12 +254,73 @@ int cuda_fail(cudaError_t e, const char* what) {
 
 // Bytes of workspace sdpa_attn_fwd needs: K/V materialised for the tensor-core path when
 // past rows or projection biases are present and no present output can hold them.
+// The tensor-core path takes the problem when the kernel fits it and the K and V views it
+// will read (the inputs, present, or the materialised copies) walk their axes alike.
+bool tc_usable(const Problem& r, sdpa_dtype dt) {
+  if (!tc_eligible(r, dt)) return false;
+  const bool needs_total = r.P > 0 || r.k_bias || r.v_bias;
+  if (needs_total && !r.present_k.p) return true;            // contiguous copies, same order
+  const View& k = needs_total ? r.present_k : r.k;
+  const View& v = needs_total ? r.present_v : r.v;
+  return tc_same_axis_order(k, v, r.B, r.Nkv, needs_total ? r.T : r.L);
+}
+
 size_t fwd_workspace(const Problem& r, sdpa_dtype dt) {
-  if (!tc_eligible(r, dt)) return 0;
+  if (!tc_usable(r, dt)) return 0;
   const bool needs_total = r.P > 0 || r.k_bias || r.v_bias;
   if (!needs_total || r.present_k.p) return 0;
   const size_t bytes = (size_t)r.B * r.Nkv * (size_t)r.T * (r.H + r.Hv) * esize(dt);
   return (bytes + 255) & ~(size_t)255;
+}
+
+size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
+
+// Bytes of workspace for the rotated copies of Q and of the new K rows; 0 without rotary.
+size_t rot_workspace(const Problem& r, const Rot& rot, sdpa_dtype dt) {
+  if (!rot.on) return 0;
+  return align256((size_t)r.B * r.Nq * r.S * r.H * esize(dt)) +
+         align256((size_t)r.B * r.Nkv * r.L * r.H * esize(dt));
+}
+
+// The problem as the attention kernels see it after the rotary step: r.q and r.k point at
+// contiguous copies at the start of `ws` (a stand-in 256-byte aligned address when ws is
+// NULL, for sizing), so every later step (present included) reads rotated Q and K.
+Problem after_rotary(const Problem& r, const Rot& rot, sdpa_dtype dt, void* ws) {
+  Problem a = r;
+  if (!rot.on) return a;
+  char* base = ws ? reinterpret_cast<char*>(ws) : reinterpret_cast<char*>((uintptr_t)256);
+  const size_t qbytes = align256((size_t)r.B * r.Nq * r.S * r.H * esize(dt));
+  a.q = View{base, (int64_t)r.Nq * r.S * r.H, (int64_t)r.S * r.H, r.H};
+  // the K copy walks its axes in V's order, so the tensor-core path can read both
+  int order[3];
+  tc_axis_order(r.v, r.B, r.Nkv, r.L, order);
+  const int64_t ext[3] = {r.L, r.Nkv, r.B};
+  int64_t str[3], cur = r.H;
+  for (int i = 0; i < 3; ++i) { str[order[i]] = cur; cur *= ext[order[i]]; }
+  a.k = View{base + qbytes, str[2], str[1], str[0]};
+  return a;
+}
+
+// GroupQueryAttention's rotary step at absolute positions: query row i of batch b sits at
+// Tv(b) - S + i and new key row j at Tv(b) - L + j, where Tv(b) = seqlens_k[b] + 1 under
+// SDPA_LEN_SEQLENS_K_I32 and T = P + L otherwise (the causal alignment's positions).
+// Writes the rotated rows to the views of after_rotary(r, rot, dt, ws).
+int run_rotary(const Problem& r, const Rot& rot, sdpa_dtype dt, void* ws, cudaStream_t st) {
+  const Problem a = after_rotary(r, rot, dt, ws);
+  RotaryPos rp{};
+  rp.mode = kRotaryAbsolute;
+  rp.cache_ld = rot.R / 2;
+  rp.max_pos = rot.max_pos;
+  rp.lens = r.r.len_kind == SDPA_LEN_SEQLENS_K_I32 ? reinterpret_cast<const int32_t*>(r.r.lens) : nullptr;
+  rp.new_rows = r.S;
+  rp.base = r.T - r.S;
+  cudaError_t e = launch_rotary(dt, r.B, r.Nq, r.S, r.H, r.q, a.q, rot.cos, rot.sin, rp, rot.R, rot.interleaved, st);
+  if (e == cudaSuccess) {
+    rp.new_rows = r.L;
+    rp.base = r.T - r.L;
+    e = launch_rotary(dt, r.B, r.Nkv, r.L, r.H, r.k, a.k, rot.cos, rot.sin, rp, rot.R, rot.interleaved, st);
+  }
+  return e == cudaSuccess ? SDPA_OK : cuda_fail(e, "rotary launch");
 }
 
 int run_concat_present(const Problem& r, sdpa_dtype dt, cudaStream_t st) {
@@ -249,25 +344,35 @@ int sdpa_validate(const sdpa_params* p, int op) {
 
 size_t sdpa_workspace_size(const sdpa_params* p, int op) {
   Problem r;
-  if (validate(p, op, &r) != SDPA_OK) return 0;
-  if (op == SDPA_OP_DECODE) return plan_decode(r.B, r.Nq, r.Nkv, r.S, r.T, r.Hv).ws_bytes;
-  return fwd_workspace(r, (sdpa_dtype)p->dtype);
+  Rot rot;
+  if (validate(p, op, &r, &rot) != SDPA_OK) return 0;
+  const sdpa_dtype dt = (sdpa_dtype)p->dtype;
+  const size_t pre = rot_workspace(r, rot, dt);
+  if (op == SDPA_OP_DECODE) return pre + plan_decode(r.B, r.Nq, r.Nkv, r.S, r.T, r.Hv).ws_bytes;
+  return pre + fwd_workspace(after_rotary(r, rot, dt, nullptr), dt);
 }
 
 int sdpa_attn_fwd(const sdpa_params* p, void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
   Problem r;
-  int rc = validate(p, SDPA_OP_FWD, &r);
+  Rot rot;
+  int rc = validate(p, SDPA_OP_FWD, &r, &rot);
   if (rc) return rc;
   const sdpa_dtype dt = (sdpa_dtype)p->dtype;
-  const size_t need = fwd_workspace(r, dt);
+  const size_t pre = rot_workspace(r, rot, dt);
+  const size_t need = pre + fwd_workspace(after_rotary(r, rot, dt, nullptr), dt);
   if (need && (!workspace || workspace_bytes < need))
     return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
   if (need && ((uintptr_t)workspace & 255u)) return fail(SDPA_ERR_ALIGNMENT, "workspace not 256-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   g_error.clear();
+  if (rot.on) {
+    if ((rc = run_rotary(r, rot, dt, workspace, st))) return rc;
+    r = after_rotary(r, rot, dt, workspace);
+    workspace = reinterpret_cast<char*>(workspace) + pre;
+  }
 
   const int64_t rows = (int64_t)r.B * r.Nq * r.S;
-  if (tc_eligible(r, dt) && rows > 0) {
+  if (tc_usable(r, dt) && rows > 0) {
     // the tensor-core kernel reads one K and one V view of T rows
     Problem a = r;
     const bool needs_total = r.P > 0 || r.k_bias || r.v_bias;
@@ -313,15 +418,23 @@ int sdpa_attn_fwd(const sdpa_params* p, void* workspace, size_t workspace_bytes,
 
 int sdpa_attn_decode(const sdpa_params* p, void* workspace, size_t workspace_bytes, sdpa_stream_t stream) {
   Problem r;
-  int rc = validate(p, SDPA_OP_DECODE, &r);
+  Rot rot;
+  int rc = validate(p, SDPA_OP_DECODE, &r, &rot);
   if (rc) return rc;
   const sdpa_dtype dt = (sdpa_dtype)p->dtype;
   const DecodePlan plan = plan_decode(r.B, r.Nq, r.Nkv, r.S, r.T, r.Hv);
-  if (plan.ws_bytes && (!workspace || workspace_bytes < plan.ws_bytes))
-    return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", plan.ws_bytes, workspace_bytes);
-  if (plan.ws_bytes && ((uintptr_t)workspace & 255u)) return fail(SDPA_ERR_ALIGNMENT, "workspace not 256-byte aligned");
+  const size_t pre = rot_workspace(r, rot, dt);
+  const size_t need = pre + plan.ws_bytes;
+  if (need && (!workspace || workspace_bytes < need))
+    return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if (need && ((uintptr_t)workspace & 255u)) return fail(SDPA_ERR_ALIGNMENT, "workspace not 256-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   g_error.clear();
+  if (rot.on) {
+    if ((rc = run_rotary(r, rot, dt, workspace, st))) return rc;
+    r = after_rotary(r, rot, dt, workspace);
+    workspace = reinterpret_cast<char*>(workspace) + pre;
+  }
   const int64_t rows = (int64_t)r.B * r.Nq * r.S;
   if (rows == 0) {
     if (r.present_k.p) return run_concat_present(r, dt, st);
@@ -335,8 +448,12 @@ int sdpa_attn_decode(const sdpa_params* p, void* workspace, size_t workspace_byt
 
 int sdpa_attn_decode_static(const sdpa_params* p, sdpa_stream_t stream) {
   Problem r;
-  int rc = validate(p, SDPA_OP_DECODE, &r);
+  Rot rot;
+  int rc = validate(p, SDPA_OP_DECODE, &r, &rot);
   if (rc) return rc;
+  if (rot.on)
+    return fail(SDPA_ERR_UNSUPPORTED, "rotary embedding needs a workspace for the rotated rows; "
+                "call sdpa_attn_decode");
   const sdpa_dtype dt = (sdpa_dtype)p->dtype;
   const DecodePlan plan = plan_decode(r.B, r.Nq, r.Nkv, r.S, r.T, r.Hv);
   if (plan.ws_bytes > decode_static_scratch_bytes())
@@ -384,13 +501,62 @@ int sdpa_kv_concat(sdpa_dtype dtype, int32_t B, int32_t N, int32_t P, int32_t L,
   return SDPA_OK;
 }
 
+int sdpa_rotary(sdpa_dtype dtype, int32_t B, int32_t N, int32_t S, int32_t D, sdpa_view x, sdpa_view y,
+                const void* cos_cache, const void* sin_cache, int64_t max_pos, const int64_t* position_ids,
+                int32_t rotary_dim, int32_t interleaved, sdpa_stream_t stream) {
+  if (dtype != SDPA_F32 && dtype != SDPA_F16 && dtype != SDPA_BF16) return fail(SDPA_ERR_INVALID, "dtype %d", dtype);
+  if (B < 0 || S < 0 || N < 1 || D < 2) return fail(SDPA_ERR_SHAPE, "bad sizes (B=%d N=%d S=%d D=%d)", B, N, S, D);
+  const int R = rotary_dim ? rotary_dim : D;
+  if (R < 2 || R > D || R % 2)
+    return fail(SDPA_ERR_INVALID, "rotary_dim %d: must be even and in [2, D=%d] (0 means D)", rotary_dim, D);
+  if (interleaved != 0 && interleaved != 1) return fail(SDPA_ERR_INVALID, "interleaved must be 0 or 1");
+  if (!cos_cache || !sin_cache) return fail(SDPA_ERR_NULL, "cos_cache / sin_cache is NULL");
+  if ((int64_t)B * S == 0) { g_error.clear(); return SDPA_OK; }      // nothing to rotate
+  if (((uintptr_t)cos_cache | (uintptr_t)sin_cache) % esize(dtype))
+    return fail(SDPA_ERR_ALIGNMENT, "caches not aligned to the element size");
+  if ((int64_t)B * N * (int64_t)S > ((int64_t)1 << 40)) return fail(SDPA_ERR_OVERFLOW, "B*N*S too large");
+  if (position_ids) {
+    if (max_pos < 1 || max_pos > ((int64_t)1 << 40)) return fail(SDPA_ERR_SHAPE, "max_pos %lld", (long long)max_pos);
+    if ((uintptr_t)position_ids & 7u) return fail(SDPA_ERR_ALIGNMENT, "position_ids not 8-byte aligned");
+  } else if (max_pos != (int64_t)B * S) {
+    return fail(SDPA_ERR_SHAPE, "without position_ids the caches are (B, S, R/2): max_pos must be B*S=%lld",
+                (long long)B * S);
+  }
+  Extent ex, ey;
+  int rc;
+  if ((rc = check_view(x, "x", dtype, B, N, S, D, true, false, &ex))) return rc;
+  if ((rc = check_view(y, "y", dtype, B, N, S, D, true, false, &ey))) return rc;
+  const bool same = x.data == y.data && x.stride_b == y.stride_b && x.stride_n == y.stride_n &&
+                    x.stride_s == y.stride_s;
+  const size_t cache_bytes = (size_t)max_pos * (R / 2) * esize(dtype);
+  if (!same && overlap(ex, ey)) return fail(SDPA_ERR_ALIAS, "y partially overlaps x");
+  if (overlap(ey, flat(cos_cache, cache_bytes, "cos_cache")) || overlap(ey, flat(sin_cache, cache_bytes, "sin_cache")) ||
+      overlap(ey, flat(position_ids, (size_t)B * S * 8, "position_ids")))
+    return fail(SDPA_ERR_ALIAS, "y overlaps a cache or position_ids");
+  g_error.clear();
+  auto cv = [](const sdpa_view& v) { return View{v.data, v.stride_b, v.stride_n, v.stride_s}; };
+  RotaryPos rp{};
+  rp.mode = position_ids ? kRotaryPositionIds : kRotaryPerToken;
+  rp.positions = position_ids;
+  rp.pos_sb = S;
+  rp.max_pos = max_pos;
+  rp.cache_ld = R / 2;
+  cudaError_t e = launch_rotary(dtype, B, N, S, D, cv(x), cv(y), cos_cache, sin_cache, rp, R, interleaved,
+                                reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "rotary launch");
+  g_kernel = "rotary";
+  return SDPA_OK;
+}
+
 int sdpa_query_status(sdpa_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-  int status = 0;
+  int status = 0, rot_status = 0;
   e = take_prefill_status(&status);
+  if (e == cudaSuccess) e = take_rotary_status(&rot_status);
   if (e != cudaSuccess) return cuda_fail(e, "status read");
   if (status) return fail(SDPA_ERR_TIMEOUT, "a bounded device wait expired (code %d)", status);
+  if (rot_status) return fail(SDPA_ERR_INVALID, "a rotary position fell outside its cos/sin cache");
   return SDPA_OK;
 }
 

@@ -20,6 +20,22 @@ cudaError_t launch_simt_fwd(const Problem& p, sdpa_dtype dt, cudaStream_t st);
 cudaError_t launch_kv_concat(sdpa_dtype dt, int B, int N, int P, int L, int D, const View& past,
                              const View& cur, const void* bias, const View& present, cudaStream_t st);
 
+// Rotary embedding: where the cache row of (batch b, row s) comes from.
+enum { kRotaryPositionIds = 0, kRotaryPerToken = 1, kRotaryAbsolute = 2 };
+struct RotaryPos {
+  int mode;
+  const int64_t* positions;  // kRotaryPositionIds: positions[b * pos_sb + s]
+  int64_t pos_sb;
+  int64_t base;              // kRotaryAbsolute: base + s, or lens[b] + 1 - new_rows + s with lens
+  const int32_t* lens;
+  int new_rows;
+  int64_t max_pos;           // rows in the caches
+  int64_t cache_ld;          // cache row length (R / 2)
+};
+cudaError_t launch_rotary(sdpa_dtype dt, int B, int N, int S, int D, const View& x, const View& y, const void* cos_c,
+                          const void* sin_c, const RotaryPos& rp, int R, int interleaved, cudaStream_t st);
+cudaError_t take_rotary_status(int* status);
+
 // Split-KV decode: partials into the workspace, then the merge kernel writes y.
 struct DecodePlan {
   int rows_per_cta;     // query rows (group heads x S) handled by one CTA

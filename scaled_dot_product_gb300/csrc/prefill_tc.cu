@@ -810,33 +810,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 4-D map over a (B, N, Seq, D) view: dim 0 = D (contiguous); dims 1..3 = seq / head /
-// batch ordered by increasing stride (size-1 axes last).  Box: 64 x 128 rows.
+// 4-D map over a (B, N, Seq, D) view: dim 0 = D (contiguous); dims 1..3 = the axes in
+// tc_axis_order.  Box: 64 x 128 rows.
 bool make_map(CUtensorMap* map, const View& v, sdpa_dtype dt, int64_t B, int64_t N, int64_t Sq, int D, int* ds,
               int* dn, int* db) {
   auto enc = encode_fn();
   if (!enc) return false;
-  struct Ax { int64_t ext, stride; int id; };
-  Ax ax[3] = {{Sq, v.ss, 0}, {N, v.sh, 1}, {B, v.sb, 2}};
-  std::stable_sort(ax, ax + 3, [](const Ax& l, const Ax& r) {
-    const bool l1 = l.ext == 1, r1 = r.ext == 1;
-    if (l1 != r1) return r1;             // size-1 axes go last
-    return l.stride < r.stride;
-  });
+  const int64_t ext[3] = {Sq, N, B};
+  const int64_t str[3] = {v.ss, v.sh, v.sb};
+  int order[3];
+  tc_axis_order(v, B, N, Sq, order);
   const int64_t es = 2;
   cuuint64_t dims[4] = {(cuuint64_t)D, 0, 0, 0};
   cuuint64_t strides[3];
   cuuint32_t box[4] = {64, 1, 1, 1};
   int64_t prev_end = (int64_t)D * es;  // bytes spanned so far
   for (int k = 0; k < 3; ++k) {
-    dims[k + 1] = (cuuint64_t)ax[k].ext;
-    int64_t sb = ax[k].stride * es;
-    if (ax[k].ext == 1) sb = ((prev_end + 15) / 16) * 16;   // never stepped: any legal stride
+    const int id = order[k];
+    dims[k + 1] = (cuuint64_t)ext[id];
+    int64_t sb = str[id] * es;
+    if (ext[id] == 1) sb = ((prev_end + 15) / 16) * 16;   // never stepped: any legal stride
     strides[k] = (cuuint64_t)sb;
-    prev_end = std::max<int64_t>(prev_end, sb * ax[k].ext);
-    if (ax[k].id == 0) { box[k + 1] = kBN; *ds = k + 1; }
-    if (ax[k].id == 1) *dn = k + 1;
-    if (ax[k].id == 2) *db = k + 1;
+    prev_end = std::max<int64_t>(prev_end, sb * ext[id]);
+    if (id == 0) { box[k + 1] = kBN; *ds = k + 1; }
+    if (id == 1) *dn = k + 1;
+    if (id == 2) *db = k + 1;
   }
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = enc(map, dt == SDPA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
@@ -889,6 +887,25 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
 }
 
 }  // namespace
+
+void tc_axis_order(const View& v, int64_t B, int64_t N, int64_t S, int order[3]) {
+  struct Ax { int64_t ext, stride; int id; };
+  Ax ax[3] = {{S, v.ss, 0}, {N, v.sh, 1}, {B, v.sb, 2}};
+  std::stable_sort(ax, ax + 3, [](const Ax& l, const Ax& r) {
+    const bool l1 = l.ext == 1, r1 = r.ext == 1;
+    if (l1 != r1) return r1;             // size-1 axes go last, in (seq, head, batch) order
+    if (l1) return false;
+    return l.stride < r.stride;
+  });
+  for (int k = 0; k < 3; ++k) order[k] = ax[k].id;
+}
+
+bool tc_same_axis_order(const View& k, const View& v, int64_t B, int64_t N, int64_t T) {
+  int ok[3], ov[3];
+  tc_axis_order(k, B, N, T, ok);
+  tc_axis_order(v, B, N, T, ov);
+  return ok[0] == ov[0] && ok[1] == ov[1] && ok[2] == ov[2];
+}
 
 bool tc_eligible(const Problem& p, sdpa_dtype dt) {
   if (dt != SDPA_F16 && dt != SDPA_BF16) return false;

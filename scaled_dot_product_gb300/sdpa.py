@@ -75,12 +75,15 @@ class sdpa_params(ctypes.Structure):
         ("len_kind", ctypes.c_int32), ("lens", ctypes.c_void_p),
         ("mask_filter_value", ctypes.c_float),
         ("softcap_before_bias", ctypes.c_int32),
+        ("rotary_cos", ctypes.c_void_p), ("rotary_sin", ctypes.c_void_p),
+        ("rotary_max_pos", ctypes.c_int64), ("rotary_dim", ctypes.c_int32),
+        ("rotary_interleaved", ctypes.c_int32),
     ]
 
 
 EXPORTED = ("sdpa_attn_fwd", "sdpa_attn_decode", "sdpa_workspace_size", "sdpa_validate",
             "sdpa_kv_concat", "sdpa_query_status", "sdpa_last_error", "sdpa_last_kernel_name",
-            "sdpa_version", "sdpa_launch_count", "sdpa_attn_decode_static")
+            "sdpa_version", "sdpa_launch_count", "sdpa_attn_decode_static", "sdpa_rotary")
 
 _lib = None
 
@@ -107,6 +110,10 @@ def lib() -> ctypes.CDLL:
         L.sdpa_kv_concat.argtypes = [ctypes.c_int] + [ctypes.c_int32] * 5 + \
             [sdpa_view, sdpa_view, ctypes.c_void_p, sdpa_view, ctypes.c_void_p]
         L.sdpa_kv_concat.restype = ctypes.c_int
+        L.sdpa_rotary.argtypes = [ctypes.c_int] + [ctypes.c_int32] * 4 + \
+            [sdpa_view, sdpa_view, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p,
+             ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p]
+        L.sdpa_rotary.restype = ctypes.c_int
         L.sdpa_query_status.argtypes = [ctypes.c_void_p]
         L.sdpa_query_status.restype = ctypes.c_int
         for f in ("sdpa_last_error", "sdpa_last_kernel_name", "sdpa_version"):
@@ -179,7 +186,8 @@ def make_params(q, k, v, *, y=None, past_k=None, past_v=None, present_k=None, pr
                 q_bias=None, k_bias=None, v_bias=None, head_sink=None, scale=None, softcap=0.0,
                 causal="none", window=-1, add_mask=None, keep_mask=None, keep_kind="none",
                 lens=None, len_kind="none", mask_filter_value=-10000.0,
-                softcap_before_bias=False) -> Tuple[sdpa_params, list]:
+                softcap_before_bias=False, rotary_cos=None, rotary_sin=None, rotary_dim=0,
+                rotary_interleaved=False) -> Tuple[sdpa_params, list]:
     """Fills sdpa_params from 4-D (B, N, S, D) views.  Returns (params, tensors to keep alive)."""
     keep: list = []
     p = sdpa_params()
@@ -212,6 +220,11 @@ def make_params(q, k, v, *, y=None, past_k=None, past_v=None, present_k=None, pr
     p.lens = _ptr(lens, keep)
     p.mask_filter_value = float(mask_filter_value)
     p.softcap_before_bias = 1 if softcap_before_bias else 0
+    if rotary_cos is not None:
+        p.rotary_cos, p.rotary_sin = _ptr(rotary_cos, keep), _ptr(rotary_sin, keep)
+        p.rotary_max_pos = rotary_cos.shape[0]
+    p.rotary_dim = int(rotary_dim)
+    p.rotary_interleaved = 1 if rotary_interleaved else 0
     return p, keep
 
 
@@ -277,6 +290,39 @@ def sdpa_kv_concat(past: Optional[torch.Tensor], cur: torch.Tensor, present: tor
     return present
 
 
+def sdpa_rotary(x: torch.Tensor, cos_cache: torch.Tensor, sin_cache: torch.Tensor,
+                position_ids: Optional[torch.Tensor] = None, *, rotary_dim: int = 0,
+                interleaved: bool = False, num_heads: Optional[int] = None,
+                y: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """RotaryEmbedding over a rank-4 (B, N, S, D) or rank-3 (B, S, N*D) tensor (num_heads
+    given).  cos/sin caches: rank-2 (max_pos, R/2) with position_ids (B, S) int64, or rank-3
+    (B, S, R/2) without.  Returns y in x's shape (`y` may be x itself)."""
+    keep: list = []
+    if x.dim() == 3:
+        if not num_heads:
+            raise ValueError("a rank-3 input needs num_heads")
+        B, S, hidden = x.shape
+        x4 = x.view(B, S, num_heads, hidden // num_heads).transpose(1, 2)
+    else:
+        x4 = x
+    B, N, S, D = x4.shape
+    if y is None:
+        y = torch.empty_like(x)
+    y4 = y.view(B, S, N, D).transpose(1, 2) if y.dim() == 3 else y
+    if cos_cache.dim() == 3:
+        max_pos = cos_cache.shape[0] * cos_cache.shape[1]
+    else:
+        max_pos = cos_cache.shape[0]
+    pos = None
+    if position_ids is not None:
+        pos = position_ids.to(torch.int64).expand(B, S).contiguous()
+    rc = lib().sdpa_rotary(_DTYPES[x.dtype], B, N, S, D, _view(x4, keep), _view(y4, keep),
+                           _ptr(cos_cache, keep), _ptr(sin_cache, keep), max_pos, _ptr(pos, keep),
+                           int(rotary_dim), 1 if interleaved else 0, _stream(stream))
+    _check(rc)
+    return y
+
+
 def sdpa_query_status(stream=None) -> int:
     return int(lib().sdpa_query_status(_stream(stream)))
 
@@ -293,7 +339,9 @@ def case_kwargs(case, present_k=None, present_v=None) -> dict:
                 causal=case.causal, window=case.window, add_mask=case.add_mask,
                 keep_mask=case.keep_mask, keep_kind=case.keep_kind, lens=case.lens,
                 len_kind=case.len_kind, mask_filter_value=case.mask_filter_value,
-                softcap_before_bias=case.softcap_before_bias)
+                softcap_before_bias=case.softcap_before_bias, rotary_cos=case.rotary_cos,
+                rotary_sin=case.rotary_sin, rotary_dim=case.rotary_dim,
+                rotary_interleaved=case.rotary_interleaved)
 
 
 def case_outputs(case):

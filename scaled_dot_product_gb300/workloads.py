@@ -50,6 +50,15 @@ def _randint(gen: torch.Generator, n: int, lo: int, hi_inclusive: int, dtype) ->
     return torch.randint(lo, hi_inclusive + 1, (n,), generator=gen, dtype=torch.int64).to(dtype)
 
 
+def rope_caches(max_pos: int, half: int, dtype, base: float = 10000.0):
+    """cos / sin input tables (max_pos, half) of RoFormer's angle schedule
+    pos * base^(-d/half), computed in float64 and converted to dtype by torch."""
+    pos = torch.arange(max_pos, dtype=torch.float64).view(-1, 1)
+    inv = base ** (-torch.arange(half, dtype=torch.float64) / half)
+    ang = pos * inv.view(1, -1)
+    return torch.cos(ang).to(dtype).contiguous(), torch.sin(ang).to(dtype).contiguous()
+
+
 def as4d(t: Optional[torch.Tensor], layout: str, n_heads: int) -> Optional[torch.Tensor]:
     """(B, N, S, D) view of a tensor stored as rank-3 (B, S, N*D) or rank-4 (B, N, S, D)."""
     if t is None:
@@ -99,6 +108,10 @@ class Case:
     len_kind: str = "none"                         # none | nonpad | keylen | seqlens_k
     mask_filter_value: float = -10000.0
     softcap_before_bias: bool = False
+    rotary_cos: Optional[torch.Tensor] = None      # (max_pos, R/2), dtype of q
+    rotary_sin: Optional[torch.Tensor] = None
+    rotary_dim: int = 0                            # R; 0 means H
+    rotary_interleaved: bool = False
     seed: int = 0
     notes: Dict[str, str] = field(default_factory=dict)
 
@@ -139,13 +152,16 @@ def make_case(name: str, *, dtype=torch.bfloat16, B=1, Nq=2, Nkv=None, S=16, L=N
               add_mask=None, add_mask_shape=None, add_mask_range=(-1.0, 0.0),
               keep_kind="none", keep_mask_shape=None, keep_density=0.8,
               len_kind="none", len_range=None, qkv_bias=None, proj_bias_std=0.02,
-              mask_filter_value=-10000.0, softcap_before_bias=False) -> Case:
+              mask_filter_value=-10000.0, softcap_before_bias=False, rotary=None, rotary_dim=0,
+              rotary_max_pos=None, rotary_base=10000.0) -> Case:
     """Draw a case.  Draw order is fixed: q, k, v, past_k, past_v, biases, sink, masks, lens.
 
     add_mask: None | "float" (uniform in add_mask_range, dtype of q, shape add_mask_shape).
     keep_kind: "bool" draws a u8 keep mask, "filter" an int32 one, both with P(keep)=keep_density
     and shape keep_mask_shape.  len_range: (lo, hi) inclusive for the per-batch lengths.
     qkv_bias: None | "q" | "qkv" (MHA projection-bias segments drawn N(0, proj_bias_std)).
+    rotary: None | "half" | "interleaved": rank-2 cos/sin caches of rotary_max_pos rows
+    (default P + L) for R = rotary_dim (0: H) channels (no random draw; see rope_caches).
     """
     Nkv = Nq if Nkv is None else Nkv
     L = S if L is None else L
@@ -188,6 +204,10 @@ def make_case(name: str, *, dtype=torch.bfloat16, B=1, Nq=2, Nkv=None, S=16, L=N
         lo, hi = len_range
         ldt = torch.int64 if len_kind == "nonpad" else torch.int32
         lens = _randint(gen, B, lo, hi, ldt)
+    rc = rs = None
+    if rotary is not None:
+        R = rotary_dim or H
+        rc, rs = rope_caches(rotary_max_pos or T, R // 2, dtype, rotary_base)
     return Case(name=name, dtype=dtype, B=B, Nq=Nq, Nkv=Nkv, S=S, L=L, P=P, H=H, Hv=Hv,
                 q=q, k=k, v=v, q_layout=q_layout, kv_layout=kv_layout, past_k=past_k,
                 past_v=past_v, want_present=want_present, q_bias=q_bias, k_bias=k_bias,
@@ -195,7 +215,45 @@ def make_case(name: str, *, dtype=torch.bfloat16, B=1, Nq=2, Nkv=None, S=16, L=N
                 window=window, head_sink=head_sink, add_mask=am, keep_mask=km,
                 keep_kind=keep_kind, lens=lens, len_kind=len_kind,
                 mask_filter_value=mask_filter_value, softcap_before_bias=softcap_before_bias,
-                seed=seed)
+                rotary_cos=rc, rotary_sin=rs, rotary_dim=rotary_dim,
+                rotary_interleaved=rotary == "interleaved", seed=seed)
+
+
+@dataclass
+class RotaryInputs:
+    """Inputs of one standalone RotaryEmbedding call."""
+    x: torch.Tensor                      # (B, N, S, D) or packed (B, S, N*D)
+    layout: str                          # "bnsh" | "bsnh"
+    N: int
+    cos: torch.Tensor                    # (max_pos, R/2) or (B, S, R/2)
+    sin: torch.Tensor
+    position_ids: Optional[torch.Tensor]  # (B, S) int64, or None with rank-3 caches
+    rotary_dim: int
+    interleaved: bool
+
+    def to(self, device) -> "RotaryInputs":
+        mv = lambda t: None if t is None else t.to(device)
+        return dataclasses.replace(self, x=mv(self.x), cos=mv(self.cos), sin=mv(self.sin),
+                                   position_ids=mv(self.position_ids))
+
+
+def make_rotary_inputs(*, B=2, N=3, S=17, D=64, dtype=torch.bfloat16, layout="bnsh", rotary_dim=0,
+                       interleaved=False, cache="ids", max_pos=None, seed=0) -> RotaryInputs:
+    """x ~ N(0, 1); cache "ids": rank-2 tables of max_pos rows (default 2*S + 5) and position
+    ids drawn uniformly in [0, max_pos); cache "per_token": rank-3 (B, S, R/2) tables."""
+    gen = torch.Generator().manual_seed(seed)
+    x = _normal(gen, (B, S, N * D) if layout == "bsnh" else (B, N, S, D), dtype)
+    half = (rotary_dim or D) // 2
+    if cache == "ids":
+        mp = max_pos or 2 * S + 5
+        cos, sin = rope_caches(mp, half, dtype)
+        pid = torch.randint(0, mp, (B, S), generator=gen, dtype=torch.int64)
+    else:
+        cos, sin = rope_caches(B * S, half, dtype)
+        cos, sin = cos.view(B, S, half), sin.view(B, S, half)
+        pid = None
+    return RotaryInputs(x=x, layout=layout, N=N, cos=cos, sin=sin, position_ids=pid,
+                        rotary_dim=rotary_dim, interleaved=interleaved)
 
 
 # ----------------------------------------------------------------------------------------

@@ -17,9 +17,23 @@ def _expand(m, case: Case):
     return m.expand(case.B, case.Nq, case.S, m.shape[-1])
 
 
+def rotated_qk(c: Case):
+    """(q, k) after GroupQueryAttention's rotary step, each rounded once to the case's
+    dtype (RotaryEmbedding's output has the input's element type); unchanged without it."""
+    q, k, v = c.views()
+    if c.rotary_cos is None:
+        return q, k
+    qpos, kpos = oracle.gqa_rotary_positions(
+        c.B, c.S, c.L, c.T, c.lens if c.len_kind == "seqlens_k" else None)
+    rq = oracle.rotary(q, c.rotary_cos, c.rotary_sin, qpos, c.rotary_dim, c.rotary_interleaved)
+    rk = oracle.rotary(k, c.rotary_cos, c.rotary_sin, kpos, c.rotary_dim, c.rotary_interleaved)
+    return oracle.round_array(rq, c.dtype), oracle.round_array(rk, c.dtype)
+
+
 def problem(case: Case) -> oracle.Problem:
     c = case.to("cpu")
-    q, k, v = c.views()
+    _, _, v = c.views()
+    q, k = rotated_qk(c)
     return oracle.Problem(
         q=q, k=k, v=v, past_k=c.past_k, past_v=c.past_v,
         q_bias=c.q_bias, k_bias=c.k_bias, v_bias=c.v_bias,
@@ -34,5 +48,6 @@ def expected_present(case: Case):
     if not case.want_present:
         return None, None
     c = case.to("cpu")
-    _, k, v = c.views()
+    _, _, v = c.views()
+    _, k = rotated_qk(c)
     return oracle.present(c.past_k, k, c.k_bias), oracle.present(c.past_v, v, c.v_bias)

@@ -191,3 +191,65 @@ def test_kv_concat_rejections():
     assert L.sdpa_kv_concat(1, 2, 2, 0, 3, 64, v(None), v(cur), None, v(cur), None) == sdpa.SDPA_ERR_ALIAS
     # D not a multiple of 8
     assert L.sdpa_kv_concat(1, 2, 2, 0, 3, 12, v(None), v(cur), None, v(pres), None) == sdpa.SDPA_ERR_UNSUPPORTED
+
+
+# ------------------------------------------------------------------ rotary embedding
+
+def _rot_args(dtype=1, B=2, N=2, S=4, D=64, R=0, inter=0, max_pos=16, ids=True, x=None, y=None):
+    keep = []
+    x = torch.zeros(B, N, S, D, dtype=torch.float16) if x is None else x
+    y = torch.zeros(B, N, S, D, dtype=torch.float16) if y is None else y
+    cos = torch.zeros(max(max_pos, 1), 32, dtype=torch.float16)
+    pid = torch.zeros(B, S, dtype=torch.int64)
+    keep += [x, y, cos, pid]
+    return (dtype, B, N, S, D, sdpa._view(x, keep), sdpa._view(y, keep), cos.data_ptr(), cos.data_ptr(),
+            max_pos, pid.data_ptr() if ids else None, R, inter, None), keep
+
+
+def test_rotary_rejections():
+    L = sdpa.lib()
+    def rc(**kw):
+        args, keep = _rot_args(**kw)
+        return L.sdpa_rotary(*args)
+    assert rc(dtype=7) == sdpa.SDPA_ERR_INVALID
+    assert rc(R=7) == sdpa.SDPA_ERR_INVALID                 # odd
+    assert rc(R=66) == sdpa.SDPA_ERR_INVALID                # wider than the head
+    assert rc(inter=2) == sdpa.SDPA_ERR_INVALID
+    assert rc(ids=False) == sdpa.SDPA_ERR_SHAPE             # rank-3 caches need max_pos == B*S
+    assert rc(max_pos=0) == sdpa.SDPA_ERR_SHAPE
+    x = torch.zeros(2, 2, 5, 64, dtype=torch.float16)
+    assert rc(x=x[:, :, :4], y=x[:, :, 1:]) == sdpa.SDPA_ERR_ALIAS   # partial overlap
+    args, keep = _rot_args()
+    args = list(args)
+    args[7] = None
+    assert L.sdpa_rotary(*args) == sdpa.SDPA_ERR_NULL
+    assert "NULL" in sdpa.sdpa_last_error()
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the behaviour without a GPU")
+def test_rotary_valid_call_without_a_gpu_fails_loudly():
+    args, keep = _rot_args()
+    assert sdpa.lib().sdpa_rotary(*args) == sdpa.SDPA_ERR_CUDA
+
+
+def test_rotary_params_validation_and_workspace():
+    cos = torch.zeros(64, 32, dtype=torch.bfloat16)
+    assert code(base(rotary_cos=cos, rotary_sin=cos)) == sdpa.SDPA_OK
+    p, keep = base(rotary_cos=cos, rotary_sin=cos)
+    p.rotary_sin = None
+    assert sdpa.sdpa_validate(p) == sdpa.SDPA_ERR_INVALID               # cos without sin
+    assert code(base(rotary_cos=cos, rotary_sin=cos, rotary_dim=5)) == sdpa.SDPA_ERR_INVALID
+    assert code(base(rotary_cos=cos, rotary_sin=cos, rotary_dim=66)) == sdpa.SDPA_ERR_INVALID
+    qb = torch.zeros(4 * 64, dtype=torch.bfloat16)
+    assert code(base(rotary_cos=cos, rotary_sin=cos, q_bias=qb)) == sdpa.SDPA_ERR_UNSUPPORTED
+    plain, k1 = base(S=1, L=1, P=40, dtype=torch.float16)
+    cos16 = torch.zeros(64, 32, dtype=torch.float16)
+    rot, k2 = base(S=1, L=1, P=40, dtype=torch.float16, rotary_cos=cos16, rotary_sin=cos16)
+    for op in (sdpa.SDPA_OP_FWD, sdpa.SDPA_OP_DECODE):
+        assert sdpa.sdpa_workspace_size(rot, op) > sdpa.sdpa_workspace_size(plain, op)
+    assert sdpa.lib().sdpa_attn_decode_static(ctypes.byref(rot), None) == sdpa.SDPA_ERR_UNSUPPORTED
+    y = torch.zeros(2, 4, 8, 64, dtype=torch.bfloat16)
+    p, keep = base(rotary_cos=cos, rotary_sin=cos)
+    p.y = sdpa._view(y, keep)
+    p.rotary_cos = p.rotary_sin = y.data_ptr()                           # output over the cache
+    assert sdpa.sdpa_validate(p) == sdpa.SDPA_ERR_ALIAS

@@ -171,6 +171,21 @@ def test_softcap_after_bias_reading():
     run_and_compare(c, "fwd")
 
 
+def test_key_and_value_views_in_different_layouts():
+    """K as (B, N, L, H) and V packed (B, L, N*Hv): the tensor-core kernel needs both views
+    to walk their axes alike, so this takes the general path; the result must not change."""
+    c = make_case("kv_mixed", dtype=torch.bfloat16, B=2, Nq=4, Nkv=2, S=150, L=150, H=64, seed=18,
+                  causal="upper_left")
+    dcase = c.to("cuda")
+    q, k, v = dcase.views()
+    v_packed = v.transpose(1, 2).contiguous().transpose(1, 2)       # same values, (s, n) swapped
+    y = sdpa.sdpa_attn_fwd(q, k, v_packed, causal="upper_left")
+    torch.cuda.synchronize()
+    assert sdpa.sdpa_query_status() == sdpa.SDPA_OK
+    err = np.abs(y.float().cpu().double().numpy() - oracle.attention(problem(c))).max()
+    assert err <= TOL[c.dtype], err
+
+
 def test_kv_concat_bit_exact_with_and_without_bias():
     for dtype in (torch.float16, torch.bfloat16, torch.float32):
         g = torch.Generator().manual_seed(17)
