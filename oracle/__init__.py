@@ -81,6 +81,9 @@ def lib():
         _lib.oracle_attention_rows.restype = ctypes.c_int
         _lib.oracle_attention_rows.argtypes = [ctypes.POINTER(_Params), ctypes.c_void_p,
                                                ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
+        _lib.oracle_qk_rows.restype = ctypes.c_int
+        _lib.oracle_qk_rows.argtypes = [ctypes.POINTER(_Params), ctypes.c_int32, ctypes.c_void_p,
+                                        ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
         _lib.oracle_present.restype = ctypes.c_int
         _lib.oracle_present.argtypes = [ctypes.c_int32] * 6 + [ctypes.POINTER(_Tensor)] * 2 + \
             [ctypes.c_void_p, ctypes.c_void_p]
@@ -192,6 +195,29 @@ def attention_rows(pr: Problem, rows: Sequence[Sequence[int]], nthreads: int = 0
     if n < 0:
         raise ValueError(f"oracle rejected the problem (code {n})")
     return out, n
+
+
+def qk_rows(pr: Problem, mode: int, rows: Sequence[Sequence[int]], nthreads: int = 0):
+    """qk output rows (class Attention, qk_matmul_output_mode = mode) of the selected query
+    rows: float64 (len(rows), T), and the thread count used."""
+    keep: list = []
+    p = _params(pr, keep)
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int64).reshape(-1, 3))
+    T = p.P + p.L
+    out = np.zeros((r.shape[0], T), dtype=np.float64)
+    n = lib().oracle_qk_rows(ctypes.byref(p), int(mode), r.ctypes.data, r.shape[0], out.ctypes.data,
+                             int(nthreads))
+    if n < 0:
+        raise ValueError(f"oracle rejected the problem (code {n})")
+    return out, n
+
+
+def qk(pr: Problem, mode: int, nthreads: int = 0) -> np.ndarray:
+    """Full qk output (B, Nq, S, T) in float64."""
+    B, Nq, _, S, L, P, _, _ = pr.dims
+    rows = np.stack(np.meshgrid(np.arange(B), np.arange(Nq), np.arange(S), indexing="ij"), -1)
+    out, _ = qk_rows(pr, mode, rows.reshape(-1, 3), nthreads)
+    return out.reshape(B, Nq, S, P + L)
 
 
 def attention(pr: Problem, nthreads: int = 0) -> np.ndarray:

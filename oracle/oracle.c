@@ -135,15 +135,31 @@ typedef struct {
   double* q;      /* H  */
   double* krow;   /* H  */
   double* vrow;   /* Hv */
-  double* s;      /* T  */
+  double* raw;    /* T: scale * <q, k_j>                                    */
+  double* nocap;  /* T: raw with every bias and mask term, before softcap   */
+  double* s;      /* T: the logit that enters the softmax                   */
   char* alive;    /* T  */
 } row_scratch;
 
-static void attention_row(const orc_params* p, int64_t b, int64_t h, int64_t i, double* y,
-                          row_scratch* w) {
-  const int64_t T = (int64_t)p->P + p->L;
+/* kv head of query head h: query heads form contiguous groups of Nq / Nkv */
+static int64_t kv_head(const orc_params* p, int64_t h) {
   const int64_t group = p->Nq / p->Nkv;
-  const int64_t kh = h / group;
+  return h / group;
+}
+
+/* softcap c * tanh(x / c); a -inf logit stays -inf */
+static double capped(const orc_params* p, double x) {
+  if (p->softcap <= 0.0 || (isinf(x) && x < 0)) return x;
+  return p->softcap * tanh(x / p->softcap);
+}
+
+/* Scores of query row (b, h, i) against every key j < T, through every stage: the scaled
+ * product, the additive mask (ai.onnx order: before softcap; softcap_before_bias: after),
+ * softcap, the mask_filter_value terms of the MultiHeadAttention masks (after softcap), and
+ * the exclusions (boolean mask, causal, window, lengths, a mask shorter than T). */
+static void score_row(const orc_params* p, int64_t b, int64_t h, int64_t i, row_scratch* w) {
+  const int64_t T = (int64_t)p->P + p->L;
+  const int64_t kh = kv_head(p, h);
 
   /* query row, with the query segment of the projection bias */
   const int64_t qo = offset4(&p->q, b, h, i);
@@ -165,10 +181,10 @@ static void attention_row(const orc_params* p, int64_t b, int64_t h, int64_t i, 
     kv_row(p, 0, b, kh, j, w->krow);
     double dot = 0.0;
     for (int64_t d = 0; d < p->H; ++d) dot += w->q[d] * w->krow[d];
-    double s = p->scale * dot;
+    const double raw = p->scale * dot;
     int excluded = 0;
 
-    /* additive mask / attention bias (before softcap in the ai.onnx stage order) */
+    /* additive mask / attention bias */
     double addv = 0.0;
     if (p->add_mask.data) {
       if (j < p->add_mask_T)
@@ -177,12 +193,9 @@ static void attention_row(const orc_params* p, int64_t b, int64_t h, int64_t i, 
       else
         excluded = 1;                        /* a mask shorter than T is padded with -inf */
     }
-    if (!p->softcap_before_bias) s += addv;
-    if (p->softcap > 0.0 && !excluded && !(isinf(s) && s < 0))
-      s = p->softcap * tanh(s / p->softcap);
-    if (p->softcap_before_bias) s += addv;
 
     /* second mask slot */
+    double filt = 0.0;                       /* mask_filter_value terms */
     if (p->keep_kind != ORC_KEEP_NONE) {
       double keep = 0.0;
       if (j < p->keep_mask_T)
@@ -190,7 +203,7 @@ static void attention_row(const orc_params* p, int64_t b, int64_t h, int64_t i, 
                                 offset4(&p->keep_mask, b, h, i) + j);
       if (keep == 0.0) {
         if (p->keep_kind == ORC_KEEP_BOOL) excluded = 1;
-        else s += p->mask_filter_value;
+        else filt += p->mask_filter_value;
       }
     }
 
@@ -198,34 +211,70 @@ static void attention_row(const orc_params* p, int64_t b, int64_t h, int64_t i, 
     if (p->causal != ORC_CAUSAL_NONE && j > pos) excluded = 1;
     if (p->window > 0 && j < pos - p->window + 1) excluded = 1;
     if (p->len_kind == ORC_LEN_NONPAD_I64 && j >= len_of(p, b)) excluded = 1;
-    if (p->len_kind == ORC_LEN_KEYLEN_I32 && j >= len_of(p, b)) s += p->mask_filter_value;
+    if (p->len_kind == ORC_LEN_KEYLEN_I32 && j >= len_of(p, b)) filt += p->mask_filter_value;
     if (p->len_kind == ORC_LEN_SEQLENS_K_I32 && j > len_of(p, b)) excluded = 1;
 
+    const double s = p->softcap_before_bias ? capped(p, raw) + addv + filt
+                                            : capped(p, raw + addv) + filt;
+    const double nocap = raw + addv + filt;
     if (isinf(s) && s < 0) excluded = 1;
-    w->s[j] = s;
+    w->raw[j] = raw;
+    w->nocap[j] = excluded ? -INFINITY : nocap;
+    w->s[j] = excluded ? -INFINITY : s;
     w->alive[j] = (char)!excluded;
   }
+}
 
-  /* softmax with the optional sink logit in the denominator */
+/* Softmax statistics of a scored row with the optional sink logit in the denominator:
+ * m = max(max_j s_j, sink), l = sum_j exp(s_j - m) + exp(sink - m).  Returns 0 when no
+ * key is admitted and there is no finite sink (the row's output is then all zeros). */
+static int softmax_stats(const orc_params* p, int64_t h, const row_scratch* w, double* mp, double* lp) {
+  const int64_t T = (int64_t)p->P + p->L;
   const int has_sink = p->head_sink != NULL;
   const double sink = has_sink ? oracle_to_double(p->bias_dtype, p->head_sink, h) : -INFINITY;
   double m = sink;
   int64_t n_alive = 0;
   for (int64_t j = 0; j < T; ++j)
     if (w->alive[j]) { ++n_alive; if (w->s[j] > m) m = w->s[j]; }
-
-  for (int64_t d = 0; d < p->Hv; ++d) y[d] = 0.0;
-  if (n_alive == 0 && !(has_sink && isfinite(sink))) return;   /* nothing admitted: zeros */
-
+  if (n_alive == 0 && !(has_sink && isfinite(sink))) return 0;   /* nothing admitted */
   double l = has_sink ? exp(sink - m) : 0.0;
+  for (int64_t j = 0; j < T; ++j)
+    if (w->alive[j]) l += exp(w->s[j] - m);
+  *mp = m;
+  *lp = l;
+  return 1;
+}
+
+static void attention_row(const orc_params* p, int64_t b, int64_t h, int64_t i, double* y,
+                          row_scratch* w) {
+  const int64_t T = (int64_t)p->P + p->L;
+  const int64_t kh = kv_head(p, h);
+  score_row(p, b, h, i, w);
+  for (int64_t d = 0; d < p->Hv; ++d) y[d] = 0.0;
+  double m, l;
+  if (!softmax_stats(p, h, w, &m, &l)) return;                  /* zeros */
   for (int64_t j = 0; j < T; ++j) {
     if (!w->alive[j]) continue;
     const double e = exp(w->s[j] - m);
-    l += e;
     kv_row(p, 1, b, kh, j, w->vrow);
     for (int64_t d = 0; d < p->Hv; ++d) y[d] += e * w->vrow[d];
   }
   for (int64_t d = 0; d < p->Hv; ++d) y[d] /= l;
+}
+
+/* The auxiliary qk output of class Attention (qk_matmul_output_mode): the T scores of
+ * row (b, h, i) at stage 0 (scale * Q K^T), 1 (with the bias and masks; an excluded key is
+ * -inf), 2 (after softcap) or 3 (softmax probabilities; an excluded key is 0). */
+static void qk_row(const orc_params* p, int32_t mode, int64_t b, int64_t h, int64_t i, double* out,
+                   row_scratch* w) {
+  const int64_t T = (int64_t)p->P + p->L;
+  score_row(p, b, h, i, w);
+  if (mode == 0) { for (int64_t j = 0; j < T; ++j) out[j] = w->raw[j]; return; }
+  if (mode == 1) { for (int64_t j = 0; j < T; ++j) out[j] = w->nocap[j]; return; }
+  if (mode == 2) { for (int64_t j = 0; j < T; ++j) out[j] = w->s[j]; return; }
+  double m, l;
+  const int any = softmax_stats(p, h, w, &m, &l);
+  for (int64_t j = 0; j < T; ++j) out[j] = (any && w->alive[j]) ? exp(w->s[j] - m) / l : 0.0;
 }
 
 typedef struct {
@@ -235,6 +284,7 @@ typedef struct {
   double* out;
   int tid, nthreads;
   int status;
+  int32_t qk_mode;    /* -1: attention output rows; 0..3: qk output rows */
 } worker_arg;
 
 static void* worker(void* argp) {
@@ -245,21 +295,28 @@ static void* worker(void* argp) {
   w.q = (double*)malloc(sizeof(double) * (size_t)(p->H + 1));
   w.krow = (double*)malloc(sizeof(double) * (size_t)(p->H + 1));
   w.vrow = (double*)malloc(sizeof(double) * (size_t)(p->Hv + 1));
+  w.raw = (double*)malloc(sizeof(double) * (size_t)(T + 1));
+  w.nocap = (double*)malloc(sizeof(double) * (size_t)(T + 1));
   w.s = (double*)malloc(sizeof(double) * (size_t)(T + 1));
   w.alive = (char*)malloc((size_t)(T + 1));
-  if (!w.q || !w.krow || !w.vrow || !w.s || !w.alive) {
+  if (!w.q || !w.krow || !w.vrow || !w.raw || !w.nocap || !w.s || !w.alive) {
     a->status = -2;
   } else {
-    for (int64_t r = a->tid; r < a->nrows; r += a->nthreads)
-      attention_row(p, a->rows[3 * r], a->rows[3 * r + 1], a->rows[3 * r + 2],
-                    a->out + r * p->Hv, &w);
+    for (int64_t r = a->tid; r < a->nrows; r += a->nthreads) {
+      if (a->qk_mode < 0)
+        attention_row(p, a->rows[3 * r], a->rows[3 * r + 1], a->rows[3 * r + 2],
+                      a->out + r * p->Hv, &w);
+      else
+        qk_row(p, a->qk_mode, a->rows[3 * r], a->rows[3 * r + 1], a->rows[3 * r + 2],
+               a->out + r * T, &w);
+    }
   }
-  free(w.q); free(w.krow); free(w.vrow); free(w.s); free(w.alive);
+  free(w.q); free(w.krow); free(w.vrow); free(w.raw); free(w.nocap); free(w.s); free(w.alive);
   return NULL;
 }
 
-int oracle_attention_rows(const orc_params* p, const int64_t* rows, int64_t nrows, double* out,
-                          int nthreads) {
+static int run_rows(const orc_params* p, int32_t qk_mode, const int64_t* rows, int64_t nrows, double* out,
+                    int nthreads) {
   if (!p || !rows || !out || nrows < 0) return -1;
   if (p->Nkv <= 0 || p->Nq % p->Nkv != 0) return -1;
   if (p->window > 0 && p->causal == ORC_CAUSAL_NONE) return -1;
@@ -277,7 +334,7 @@ int oracle_attention_rows(const orc_params* p, const int64_t* rows, int64_t nrow
   if (!th || !args) { free(th); free(args); return -2; }
   int started = 0;
   for (int t = 0; t < nthreads; ++t) {
-    args[t] = (worker_arg){p, rows, nrows, out, t, nthreads, 0};
+    args[t] = (worker_arg){p, rows, nrows, out, t, nthreads, 0, qk_mode};
     if (pthread_create(&th[t], NULL, worker, &args[t]) != 0) break;
     ++started;
   }
@@ -287,7 +344,7 @@ int oracle_attention_rows(const orc_params* p, const int64_t* rows, int64_t nrow
   if (started < nthreads) {
     /* finish the rows of threads that could not be started on this thread */
     for (int t = started; t < nthreads; ++t) {
-      worker_arg a = {p, rows, nrows, out, t, nthreads, 0};
+      worker_arg a = {p, rows, nrows, out, t, nthreads, 0, qk_mode};
       worker(&a);
       if (a.status) status = a.status;
     }
@@ -295,6 +352,17 @@ int oracle_attention_rows(const orc_params* p, const int64_t* rows, int64_t nrow
   free(th);
   free(args);
   return status ? status : nthreads;
+}
+
+int oracle_attention_rows(const orc_params* p, const int64_t* rows, int64_t nrows, double* out,
+                          int nthreads) {
+  return run_rows(p, -1, rows, nrows, out, nthreads);
+}
+
+int oracle_qk_rows(const orc_params* p, int32_t mode, const int64_t* rows, int64_t nrows, double* out,
+                   int nthreads) {
+  if (mode < 0 || mode > 3) return -1;
+  return run_rows(p, mode, rows, nrows, out, nthreads);
 }
 
 /* ---- rounding of a double array to an element type (once, to nearest even) ---- */

@@ -82,6 +82,15 @@ typedef struct {
 int oracle_attention_rows(const orc_params* p, const int64_t* rows, int64_t nrows, double* out,
                           int nthreads);
 
+/* The auxiliary qk output of class Attention (qk_matmul_output_mode) for selected query
+ * rows: out receives nrows * (P+L) doubles, the scores of each row at stage `mode`:
+ * 0 = scale * Q K^T; 1 = with the additive bias and masks (an excluded key is -inf);
+ * 2 = after softcap (the logits of the softmax); 3 = softmax probabilities, the sink in the
+ * denominator (an excluded key is 0; a row with nothing admitted is all 0).
+ * Returns the number of threads used, or a negative value on a bad argument. */
+int oracle_qk_rows(const orc_params* p, int32_t mode, const int64_t* rows, int64_t nrows, double* out,
+                   int nthreads);
+
 /* Present tensor (B, N, P+L, D), contiguous, in dtype: past positions followed by the new
  * ones (new + bias, rounded once to dtype, when bias is given). */
 int oracle_present(int32_t dtype, int32_t B, int32_t N, int32_t P, int32_t L, int32_t D,

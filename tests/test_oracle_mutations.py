@@ -10,17 +10,21 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SRC = os.path.join(ROOT, "oracle", "oracle.c")
 
 MUTATIONS = {
-    "interleaved_group_mapping": ("const int64_t kh = h / group;", "const int64_t kh = h % p->Nkv;"),
+    "interleaved_group_mapping": ("return h / group;", "return h % p->Nkv;"),
     "causal_off_by_one": ("ORC_CAUSAL_NONE && j > pos)", "ORC_CAUSAL_NONE && j >= pos)"),
     "window_off_by_one": ("j < pos - p->window + 1)", "j < pos - p->window)"),
-    "dropped_scale": ("double s = p->scale * dot;", "double s = dot;"),
+    "dropped_scale": ("const double raw = p->scale * dot;", "const double raw = dot;"),
     "sink_left_out_of_denominator": ("double l = has_sink ? exp(sink - m) : 0.0;", "double l = 0.0;"),
     "nonpad_off_by_one": ("ORC_LEN_NONPAD_I64 && j >= len_of(p, b))", "ORC_LEN_NONPAD_I64 && j > len_of(p, b))"),
-    "mask_sign": ("if (!p->softcap_before_bias) s += addv;", "if (!p->softcap_before_bias) s -= addv;"),
+    "mask_sign": (": capped(p, raw + addv) + filt;", ": capped(p, raw - addv) + filt;"),
     "q_bias_segment_ignores_head": ("p->q_bias, h * p->H + d)", "p->q_bias, d)"),
-    "filter_as_exclusion": ("ORC_LEN_KEYLEN_I32 && j >= len_of(p, b)) s += p->mask_filter_value;",
+    "filter_as_exclusion": ("ORC_LEN_KEYLEN_I32 && j >= len_of(p, b)) filt += p->mask_filter_value;",
                             "ORC_LEN_KEYLEN_I32 && j >= len_of(p, b)) excluded = 1;"),
-    "softcap_missing_outer_factor": ("s = p->softcap * tanh(s / p->softcap);", "s = tanh(s / p->softcap);"),
+    "softcap_missing_outer_factor": ("return p->softcap * tanh(x / p->softcap);", "return tanh(x / p->softcap);"),
+    "qk_mode0_includes_bias": ("out[j] = w->raw[j]; return;", "out[j] = w->nocap[j]; return;"),
+    "qk_mode1_keeps_excluded_scores": ("w->nocap[j] = excluded ? -INFINITY : nocap;", "w->nocap[j] = nocap;"),
+    "qk_mode2_before_softcap": ("out[j] = w->s[j]; return;", "out[j] = w->nocap[j]; return;"),
+    "qk_mode3_unnormalised": ("exp(w->s[j] - m) / l : 0.0;", "exp(w->s[j] - m) : 0.0;"),
     "lower_right_shift": ("pos = valid_total - p->S + i;", "pos = valid_total - p->S + i + 1;"),
     "f16_exponent_bias": ("e - 25);", "e - 24);"),
     "past_not_first": ("if (j < p->P) {", "if (j >= p->L) {"),

@@ -525,3 +525,87 @@ def test_gqa_rotary_positions():
     assert qp.tolist() == [[5], [9]] and kp.tolist() == [[5], [9]]
     qp, kp = oracle.gqa_rotary_positions(1, 3, 4, 10)
     assert qp.tolist() == [[7, 8, 9]] and kp.tolist() == [[6, 7, 8, 9]]
+
+
+# ---------------------------------------------------------------- qk output (class Attention, qk_matmul_output_mode)
+
+def _qk_case(seed=60, **kw):
+    B, Nq, Nkv, S, T, H = 2, 4, 2, 6, 9, 8
+    q, k, v = rnd(B, Nq, S, H, seed=seed), rnd(B, Nkv, T, H, seed=seed + 1), rnd(B, Nkv, T, H, seed=seed + 2)
+    return q, k, v
+
+
+def _qk_expand(k, Nq):
+    return k.repeat_interleave(Nq // k.shape[1], dim=1)
+
+
+def test_qk_mode0_is_the_scaled_product_whatever_the_masks():
+    q, k, v = _qk_case()
+    mask = rnd(2, 1, 6, 7, seed=63)                        # shorter than T: padded
+    got = oracle.qk(Problem(q=q, k=k, v=v, scale=0.3, softcap=2.0, causal=oracle.CAUSAL_UPPER_LEFT,
+                            add_mask=mask.expand(2, 4, 6, 7)), 0)
+    want = 0.3 * torch.matmul(q, _qk_expand(k, 4).transpose(-1, -2))
+    np.testing.assert_allclose(got, want.numpy(), rtol=0, atol=1e-12)
+
+
+def test_qk_mode1_adds_the_bias_and_excludes_with_minus_inf():
+    q, k, v = _qk_case(seed=64)
+    mask = rnd(2, 1, 6, 7, seed=67)
+    pr = Problem(q=q, k=k, v=v, scale=0.3, causal=oracle.CAUSAL_UPPER_LEFT, add_mask=mask.expand(2, 4, 6, 7))
+    raw = 0.3 * torch.matmul(q, _qk_expand(k, 4).transpose(-1, -2))
+    want = raw.clone()
+    want[..., :7] += mask
+    want[..., 7:] = -math.inf                             # the padding of a short mask
+    want = want.masked_fill(torch.ones(6, 9).triu(1).bool(), -math.inf)   # j > i
+    np.testing.assert_array_equal(np.isinf(oracle.qk(pr, 1)), np.isinf(want.numpy()))
+    np.testing.assert_allclose(oracle.qk(pr, 1), want.numpy(), rtol=0, atol=1e-12)
+
+
+def test_qk_mode2_is_softcap_of_mode1_and_mode3_is_its_softmax():
+    q, k, v = _qk_case(seed=68)
+    pr = Problem(q=q, k=k, v=v, scale=1.7, softcap=1.5, causal=oracle.CAUSAL_LOWER_RIGHT)
+    m1, m2, m3 = oracle.qk(pr, 1), oracle.qk(pr, 2), oracle.qk(pr, 3)
+    fin = np.isfinite(m1)
+    np.testing.assert_array_equal(fin, np.isfinite(m2))
+    np.testing.assert_allclose(m2[fin], 1.5 * np.tanh(m1[fin] / 1.5), rtol=0, atol=1e-12)
+    want3 = torch.softmax(torch.from_numpy(m2), dim=-1).numpy()
+    np.testing.assert_allclose(m3, want3, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(m3.sum(-1), 1.0, atol=1e-12)
+
+
+def test_qk_probabilities_times_values_give_the_output():
+    """Y = P V: the mode-3 output is the matrix the attention output averages V with,
+    here with past rows, GQA, an additive mask, a window and a sink."""
+    B, Nq, Nkv, S, L, P, H = 2, 4, 2, 5, 5, 4, 8
+    q = rnd(B, Nq, S, H, seed=70)
+    k, v = rnd(B, Nkv, L, H, seed=71), rnd(B, Nkv, L, H, seed=72)
+    pk, pv = rnd(B, Nkv, P, H, seed=73), rnd(B, Nkv, P, H, seed=74)
+    sink = rnd(Nq, seed=75)
+    mask = rnd(B, Nq, S, P + L, seed=76)
+    pr = Problem(q=q, k=k, v=v, past_k=pk, past_v=pv, causal=oracle.CAUSAL_LOWER_RIGHT, window=3,
+                 head_sink=sink, add_mask=mask)
+    probs = oracle.qk(pr, 3)
+    vt = _qk_expand(torch.cat([pv, v], 2), Nq).numpy()
+    np.testing.assert_allclose(np.einsum("bhst,bhtd->bhsd", probs, vt), oracle.attention(pr), atol=1e-12)
+    # the sink takes the rest of the mass: sum_j p_j + e^sink / (sum_j e^s_j + e^sink) = 1
+    logits = oracle.qk(pr, 2)
+    e = np.exp(logits)                                     # exp(-inf) = 0 for excluded keys
+    es = np.exp(sink.numpy())[None, :, None]
+    np.testing.assert_allclose(probs.sum(-1) + es / (e.sum(-1) + es), 1.0, atol=1e-12)
+    assert (probs.sum(-1) < 1.0).all()
+
+
+def test_qk_fully_excluded_row_and_filter_values():
+    q, k, v = _qk_case(seed=80)
+    keep = torch.ones(2, 4, 6, 9, dtype=torch.uint8)
+    keep[0, 1, 2] = 0                                     # one row with nothing admitted
+    pr = Problem(q=q, k=k, v=v, keep_mask=keep, keep_kind=oracle.KEEP_BOOL)
+    np.testing.assert_array_equal(oracle.qk(pr, 1)[0, 1, 2], -np.inf)
+    np.testing.assert_array_equal(oracle.qk(pr, 3)[0, 1, 2], 0.0)
+    # MultiHeadAttention key padding adds mask_filter_value instead of excluding
+    lens = torch.tensor([4, 9], dtype=torch.int32)
+    pr = Problem(q=q, k=k, v=v, len_kind=oracle.LEN_KEYLEN_I32, lens=lens, mask_filter_value=-50.0)
+    raw, m1 = oracle.qk(pr, 0), oracle.qk(pr, 1)
+    np.testing.assert_allclose(m1[0, :, :, 4:], raw[0, :, :, 4:] - 50.0, atol=1e-12)
+    np.testing.assert_array_equal(m1[0, :, :, :4], raw[0, :, :, :4])
+    np.testing.assert_array_equal(m1[1], raw[1])
