@@ -203,7 +203,7 @@ def with_rope(case: Case) -> Case:
 
 
 def measure_native(idx: int, steps: int, warmup: int, barrier, with_e2e: bool = True, batch=None,
-                   rope: bool = False):
+                   rope: bool = False, qk_mode=None):
     from scaled_dot_product_gb300 import sdpa
     case_cpu = workload(idx, batch=batch)
     if rope:
@@ -213,7 +213,11 @@ def measure_native(idx: int, steps: int, warmup: int, barrier, with_e2e: bool = 
     ws = sdpa.case_workspace(case, op)
     outs = sdpa.case_outputs(case)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
-    run = lambda: sdpa.run_case(case, op, outputs=outs, workspace=ws)
+    extra = {}
+    if qk_mode is not None:
+        extra = dict(qk_out=torch.empty(case.B, case.Nq, case.S, case.T, dtype=torch.float32, device="cuda"),
+                     qk_mode=qk_mode)
+    run = lambda: sdpa.run_case(case, op, outputs=outs, workspace=ws, **extra)
     run()
     torch.cuda.synchronize()
     kernel = sdpa.sdpa_last_kernel_name()
@@ -499,6 +503,24 @@ def main():
             del r
             torch.cuda.empty_cache()
         line["rotary"] = nxt
+        # the auxiliary qk output (qk_matmul_output_mode 0 and 3) on the GQA prefill: the
+        # output write is the added work; GB/s counts its bytes over the added time
+        if idx == 2:
+            qkl = []
+            for mode in (0, 3):
+                r = measure_native(2, max(5, min(a.steps // 2, 200)), warmup, barrier, with_e2e=False, qk_mode=mode)
+                m = statistics.mean(r["ms"])
+                c = r["case"]
+                out_bytes = c.B * c.Nq * c.S * c.T * 4
+                extra_ms = m - ms
+                gbs = out_bytes / (extra_ms * 1e-3) / 1e9 if extra_ms > 0 else None
+                qkl.append({"workload": c.name + f"_qk_mode{mode}", "ms_per_step": m, "qk_extra_ms": extra_ms,
+                            "qk_out_bytes": out_bytes, "qk_GBps_over_extra_time": gbs,
+                            "frac_of_hbm": None if gbs is None else gbs / hbm,
+                            "kernel": r["kernel"], "gpu_launches": r["launches"]})
+                del r
+                torch.cuda.empty_cache()
+            line["qk_output"] = qkl
     print(json.dumps(line))
 
 

@@ -156,6 +156,14 @@ typedef struct {
   int64_t rotary_max_pos;
   int32_t rotary_dim;
   int32_t rotary_interleaved;
+  /* Auxiliary qk output of class Attention (qk_matmul_output_mode), written by
+   * sdpa_attn_fwd when qk_out.data != NULL: a (B, Nq, S, P+L) FLOAT view (last dimension
+   * contiguous) of the scores at stage qk_mode: 0 = scale * Q K^T; 1 = with the additive
+   * bias and every mask (an excluded key is -inf); 2 = after softcap (the softmax's
+   * logits); 3 = the softmax probabilities, the sink in the denominator (an excluded key is
+   * 0).  The decode entry points reject it (SDPA_ERR_UNSUPPORTED). */
+  sdpa_view qk_out;
+  int32_t qk_mode;
 } sdpa_params;
 
 /* Which entry point a workspace query is for. */

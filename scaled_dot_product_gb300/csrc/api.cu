@@ -144,6 +144,11 @@ int validate(const sdpa_params* p, int op, Problem* pr, Rot* rot = nullptr) {
     return fail(SDPA_ERR_SHAPE, "P=%d past rows but past_k/past_v absent", p->P);
   if (p->P == 0 && (p->past_k.data || p->past_v.data))
     return fail(SDPA_ERR_SHAPE, "past_k/past_v given with P=0");
+  if (p->qk_out.data) {
+    if (op == SDPA_OP_DECODE)
+      return fail(SDPA_ERR_UNSUPPORTED, "the qk output is written by sdpa_attn_fwd only");
+    if (p->qk_mode < 0 || p->qk_mode > 3) return fail(SDPA_ERR_INVALID, "qk_mode %d: must be 0..3", p->qk_mode);
+  }
   if ((p->rotary_cos == nullptr) != (p->rotary_sin == nullptr))
     return fail(SDPA_ERR_INVALID, "rotary_cos and rotary_sin must be given together");
   const bool rot_on = p->rotary_cos != nullptr;
@@ -180,6 +185,8 @@ int validate(const sdpa_params* p, int op, Problem* pr, Rot* rot = nullptr) {
   if ((rc = check_view(p->present_k, "present_k", dt, p->B, p->Nkv, T, p->H, false, false, &eprk))) return rc;
   if ((rc = check_view(p->present_v, "present_v", dt, p->B, p->Nkv, T, p->Hv, false, false, &eprv))) return rc;
   if ((rc = check_view(p->y, "y", dt, p->B, p->Nq, p->S, p->Hv, true, false, &ey))) return rc;
+  Extent eqk;
+  if ((rc = check_view(p->qk_out, "qk_out", SDPA_F32, p->B, p->Nq, p->S, T, false, false, &eqk))) return rc;
   const int mdt = p->add_mask.data ? p->add_mask_dtype : SDPA_F32;
   if ((rc = check_view(p->add_mask, "add_mask", mdt, p->B, p->Nq, p->S, p->add_mask_T, false, true, &eam))) return rc;
   // keep masks are u8 or i32: reuse the f32/f16 element sizes for the extent
@@ -207,12 +214,13 @@ int validate(const sdpa_params* p, int op, Problem* pr, Rot* rot = nullptr) {
                            flat(p->lens, (size_t)p->B * (p->len_kind == SDPA_LEN_NONPAD_I64 ? 8 : 4), "lens"),
                            flat(p->rotary_cos, (size_t)p->rotary_max_pos * (rot_R / 2) * esize(dt), "rotary_cos"),
                            flat(p->rotary_sin, (size_t)p->rotary_max_pos * (rot_R / 2) * esize(dt), "rotary_sin")};
-  for (const Extent& o : {ey, eprk, eprv}) {
+  for (const Extent& o : {ey, eprk, eprv, eqk}) {
     for (const Extent& in : inputs)
       if (overlap(o, in)) return fail(SDPA_ERR_ALIAS, "output %s overlaps input %s", o.name, in.name);
   }
-  if (overlap(ey, eprk) || overlap(ey, eprv) || overlap(eprk, eprv))
-    return fail(SDPA_ERR_ALIAS, "outputs y / present_k / present_v overlap");
+  if (overlap(ey, eprk) || overlap(ey, eprv) || overlap(eprk, eprv) || overlap(eqk, ey) || overlap(eqk, eprk) ||
+      overlap(eqk, eprv))
+    return fail(SDPA_ERR_ALIAS, "outputs y / present_k / present_v / qk_out overlap");
 
   // resolved problem
   Problem& r = *pr;
@@ -312,15 +320,27 @@ int run_rotary(const Problem& r, const Rot& rot, sdpa_dtype dt, void* ws, cudaSt
   rp.cache_ld = rot.R / 2;
   rp.max_pos = rot.max_pos;
   rp.lens = r.r.len_kind == SDPA_LEN_SEQLENS_K_I32 ? reinterpret_cast<const int32_t*>(r.r.lens) : nullptr;
-  rp.new_rows = r.S;
-  rp.base = r.T - r.S;
-  cudaError_t e = launch_rotary(dt, r.B, r.Nq, r.S, r.H, r.q, a.q, rot.cos, rot.sin, rp, rot.R, rot.interleaved, st);
-  if (e == cudaSuccess) {
-    rp.new_rows = r.L;
-    rp.base = r.T - r.L;
-    e = launch_rotary(dt, r.B, r.Nkv, r.L, r.H, r.k, a.k, rot.cos, rot.sin, rp, rot.R, rot.interleaved, st);
-  }
+  RotaryJob jobs[2];
+  jobs[0] = RotaryJob{r.q, a.q, r.B, r.Nq, r.S, rp};
+  jobs[0].rp.new_rows = r.S;
+  jobs[0].rp.base = r.T - r.S;
+  jobs[1] = RotaryJob{r.k, a.k, r.B, r.Nkv, r.L, rp};
+  jobs[1].rp.new_rows = r.L;
+  jobs[1].rp.base = r.T - r.L;
+  const cudaError_t e = launch_rotary(dt, jobs, 2, r.H, rot.cos, rot.sin, rot.R, rot.interleaved, st);
   return e == cudaSuccess ? SDPA_OK : cuda_fail(e, "rotary launch");
+}
+
+// The qk output (class Attention's qk_matmul_output) after the attention launch.
+thread_local std::string g_kernel_pair;
+int run_qk(const Problem& r, const View* k_total, const sdpa_params* p, sdpa_dtype dt, cudaStream_t st) {
+  const View out{p->qk_out.data, p->qk_out.stride_b, p->qk_out.stride_n, p->qk_out.stride_s};
+  const char* name = "";
+  const cudaError_t e = launch_qk(r, k_total, out, p->qk_mode, dt, st, &name);
+  if (e != cudaSuccess) return cuda_fail(e, "qk output launch");
+  g_kernel_pair = std::string(g_kernel) + "+" + name;
+  g_kernel = g_kernel_pair.c_str();
+  return SDPA_OK;
 }
 
 int run_concat_present(const Problem& r, sdpa_dtype dt, cudaStream_t st) {
@@ -400,6 +420,7 @@ int sdpa_attn_fwd(const sdpa_params* p, void* workspace, size_t workspace_bytes,
     cudaError_t e = launch_prefill_tc(a, dt, st, &name);
     if (e != cudaSuccess) return cuda_fail(e, "prefill_tc launch");
     g_kernel = name;
+    if (p->qk_out.data && (rc = run_qk(r, &a.k, p, dt, st))) return rc;
     return SDPA_OK;
   }
 
@@ -412,6 +433,11 @@ int sdpa_attn_fwd(const sdpa_params* p, void* workspace, size_t workspace_bytes,
     cudaError_t e = launch_simt_fwd(a, dt, st);
     if (e != cudaSuccess) return cuda_fail(e, "simt_fwd launch");
     g_kernel = dt == SDPA_F32 ? "simt_fwd_f32" : dt == SDPA_F16 ? "simt_fwd_f16" : "simt_fwd_bf16";
+    if (p->qk_out.data) {
+      // one view of all T key rows, where the inputs already hold one
+      const View* kt = (r.P == 0 && !r.k_bias) ? &r.k : (r.present_k.p ? &r.present_k : nullptr);
+      if ((rc = run_qk(r, kt, p, dt, st))) return rc;
+    }
   }
   return SDPA_OK;
 }
@@ -541,7 +567,8 @@ int sdpa_rotary(sdpa_dtype dtype, int32_t B, int32_t N, int32_t S, int32_t D, sd
   rp.pos_sb = S;
   rp.max_pos = max_pos;
   rp.cache_ld = R / 2;
-  cudaError_t e = launch_rotary(dtype, B, N, S, D, cv(x), cv(y), cos_cache, sin_cache, rp, R, interleaved,
+  const RotaryJob job{cv(x), cv(y), B, N, S, rp};
+  cudaError_t e = launch_rotary(dtype, &job, 1, D, cos_cache, sin_cache, R, interleaved,
                                 reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "rotary launch");
   g_kernel = "rotary";
@@ -551,10 +578,12 @@ int sdpa_rotary(sdpa_dtype dtype, int32_t B, int32_t N, int32_t S, int32_t D, sd
 int sdpa_query_status(sdpa_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-  int status = 0, rot_status = 0;
+  int status = 0, rot_status = 0, qk_status = 0;
   e = take_prefill_status(&status);
   if (e == cudaSuccess) e = take_rotary_status(&rot_status);
+  if (e == cudaSuccess) e = take_qk_status(&qk_status);
   if (e != cudaSuccess) return cuda_fail(e, "status read");
+  if (!status) status = qk_status;
   if (status) return fail(SDPA_ERR_TIMEOUT, "a bounded device wait expired (code %d)", status);
   if (rot_status) return fail(SDPA_ERR_INVALID, "a rotary position fell outside its cos/sin cache");
   return SDPA_OK;

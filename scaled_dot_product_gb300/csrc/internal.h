@@ -32,9 +32,22 @@ struct RotaryPos {
   int64_t max_pos;           // rows in the caches
   int64_t cache_ld;          // cache row length (R / 2)
 };
-cudaError_t launch_rotary(sdpa_dtype dt, int B, int N, int S, int D, const View& x, const View& y, const void* cos_c,
-                          const void* sin_c, const RotaryPos& rp, int R, int interleaved, cudaStream_t st);
+// One rotation: (B, N, S, D) view x into y, cache rows chosen by rp.
+struct RotaryJob {
+  View x, y;
+  int B, N, S;
+  RotaryPos rp;
+};
+// njobs (1 or 2) jobs sharing D, the caches, R and the pair layout.
+cudaError_t launch_rotary(sdpa_dtype dt, const RotaryJob* jobs, int njobs, int D, const void* cos_c,
+                          const void* sin_c, int R, int interleaved, cudaStream_t st);
 cudaError_t take_rotary_status(int* status);
+
+// Auxiliary qk output (B, Nq, S, T) fp32 at stage `mode` (0..3).  k_total: one view of all
+// T key rows when one exists (enables the tensor-core kernel), else nullptr.
+cudaError_t launch_qk(const Problem& p, const View* k_total, const View& out, int mode, sdpa_dtype dt,
+                      cudaStream_t st, const char** name);
+cudaError_t take_qk_status(int* status);
 
 // Split-KV decode: partials into the workspace, then the merge kernel writes y.
 struct DecodePlan {

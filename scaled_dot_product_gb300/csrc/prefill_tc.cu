@@ -965,6 +965,13 @@ cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, 
   return bf ? launch_t<64, true>(tq, tk, tv, a, units, st) : launch_t<64, false>(tq, tk, tv, a, units, st);
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() { return encode_fn(); }
+
+bool tc_make_map(CUtensorMap* map, const View& v, sdpa_dtype dt, int64_t B, int64_t N, int64_t Sq, int D, int* ds,
+                 int* dn, int* db) {
+  return make_map(map, v, dt, B, N, Sq, D, ds, dn, db);
+}
+
 cudaError_t take_prefill_status(int* status) {
   int v = 0;
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_prefill_status, sizeof v);

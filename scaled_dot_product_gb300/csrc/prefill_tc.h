@@ -1,6 +1,8 @@
 // Tensor-core (tcgen05 / TMEM / TMA) prefill path.
 #pragma once
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 
 namespace sdpa {
@@ -16,6 +18,13 @@ bool tc_eligible(const Problem& p, sdpa_dtype dt);
 // must share it (tc_same_axis_order).
 void tc_axis_order(const View& v, int64_t B, int64_t N, int64_t S, int order[3]);
 bool tc_same_axis_order(const View& k, const View& v, int64_t B, int64_t N, int64_t T);
+
+// Driver entry point of cuTensorMapEncodeTiled (nullptr when unavailable), and the 4-D
+// 16-bit map over a (B, N, Seq, D) view the kernels use (box 64 x 128 rows, 128-byte
+// swizzle); ds / dn / db receive the map dimension of seq / head / batch.
+PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn();
+bool tc_make_map(CUtensorMap* map, const View& v, sdpa_dtype dt, int64_t B, int64_t N, int64_t Sq, int D, int* ds,
+                 int* dn, int* db);
 
 // Launches the fused kernel; p.k / p.v must hold all T key rows (P == 0, no kv bias).
 cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, const char** name);

@@ -78,6 +78,7 @@ class sdpa_params(ctypes.Structure):
         ("rotary_cos", ctypes.c_void_p), ("rotary_sin", ctypes.c_void_p),
         ("rotary_max_pos", ctypes.c_int64), ("rotary_dim", ctypes.c_int32),
         ("rotary_interleaved", ctypes.c_int32),
+        ("qk_out", sdpa_view), ("qk_mode", ctypes.c_int32),
     ]
 
 
@@ -187,7 +188,7 @@ def make_params(q, k, v, *, y=None, past_k=None, past_v=None, present_k=None, pr
                 causal="none", window=-1, add_mask=None, keep_mask=None, keep_kind="none",
                 lens=None, len_kind="none", mask_filter_value=-10000.0,
                 softcap_before_bias=False, rotary_cos=None, rotary_sin=None, rotary_dim=0,
-                rotary_interleaved=False) -> Tuple[sdpa_params, list]:
+                rotary_interleaved=False, qk_out=None, qk_mode=0) -> Tuple[sdpa_params, list]:
     """Fills sdpa_params from 4-D (B, N, S, D) views.  Returns (params, tensors to keep alive)."""
     keep: list = []
     p = sdpa_params()
@@ -225,6 +226,8 @@ def make_params(q, k, v, *, y=None, past_k=None, past_v=None, present_k=None, pr
         p.rotary_max_pos = rotary_cos.shape[0]
     p.rotary_dim = int(rotary_dim)
     p.rotary_interleaved = 1 if rotary_interleaved else 0
+    p.qk_out = _view(qk_out, keep)
+    p.qk_mode = int(qk_mode)
     return p, keep
 
 
@@ -357,12 +360,13 @@ def case_outputs(case):
     return y_store, y4, pk, pv
 
 
-def run_case(case, op: str = "fwd", outputs=None, workspace=None, stream=None):
-    """Runs a device-resident case; returns (y in the query's layout, present_k, present_v)."""
+def run_case(case, op: str = "fwd", outputs=None, workspace=None, stream=None, **extra):
+    """Runs a device-resident case; returns (y in the query's layout, present_k, present_v).
+    `extra` adds make_params keywords (e.g. qk_out / qk_mode)."""
     q, k, v = case.views()
     y_store, y4, pk, pv = outputs if outputs is not None else case_outputs(case)
     entry = sdpa_attn_decode if op == "decode" else sdpa_attn_fwd
-    entry(q, k, v, y=y4, workspace=workspace, stream=stream, **case_kwargs(case, pk, pv))
+    entry(q, k, v, y=y4, workspace=workspace, stream=stream, **case_kwargs(case, pk, pv), **extra)
     return y_store, pk, pv
 
 

@@ -253,3 +253,21 @@ def test_rotary_params_validation_and_workspace():
     p.y = sdpa._view(y, keep)
     p.rotary_cos = p.rotary_sin = y.data_ptr()                           # output over the cache
     assert sdpa.sdpa_validate(p) == sdpa.SDPA_ERR_ALIAS
+
+
+# ------------------------------------------------------------------ qk output
+
+def test_qk_output_validation():
+    qk = torch.zeros(2, 4, 8, 8, dtype=torch.float32)
+    assert code(base(qk_out=qk, qk_mode=3)) == sdpa.SDPA_OK
+    assert code(base(qk_out=qk, qk_mode=4)) == sdpa.SDPA_ERR_INVALID
+    assert code(base(qk_out=qk, qk_mode=-1)) == sdpa.SDPA_ERR_INVALID
+    assert code(base(qk_out=qk), sdpa.SDPA_OP_DECODE) == sdpa.SDPA_ERR_UNSUPPORTED
+    # qk output over an input
+    q = torch.zeros(2, 4, 8, 64, dtype=torch.bfloat16)
+    k = torch.zeros(2, 2, 8, 64, dtype=torch.bfloat16)
+    v = torch.zeros(2, 2, 8, 64, dtype=torch.bfloat16)
+    y = torch.zeros(2, 4, 8, 64, dtype=torch.bfloat16)
+    over = q.view(torch.float32)[..., :8]                    # inside q's bytes
+    p, keep = sdpa.make_params(q, k, v, y=y, qk_out=over)
+    assert sdpa.sdpa_validate(p) == sdpa.SDPA_ERR_ALIAS

@@ -77,6 +77,9 @@ STANDALONE = [
     dict(dtype=torch.bfloat16, layout="bsnh", interleaved=True, rotary_dim=48, cache="ids"),
     dict(dtype=torch.float16, layout="bnsh", interleaved=False, rotary_dim=16, cache="per_token", D=128),
     dict(dtype=torch.float32, layout="bsnh", interleaved=True, rotary_dim=8, cache="ids", D=32),
+    # R/2 not a multiple of a 16-byte vector: the scalar kernel
+    dict(dtype=torch.float16, layout="bnsh", interleaved=False, rotary_dim=12, cache="ids"),
+    dict(dtype=torch.bfloat16, layout="bsnh", interleaved=True, rotary_dim=6, cache="per_token"),
 ]
 
 
@@ -106,6 +109,24 @@ def test_standalone_rotary_in_place_and_empty():
     e = torch.empty(0, 4, 5, 128, dtype=torch.bfloat16, device="cuda")
     sdpa.sdpa_rotary(e, d.cos, d.sin, torch.zeros(0, 5, dtype=torch.int64, device="cuda"))
     assert sdpa.sdpa_query_status() == sdpa.SDPA_OK
+
+
+def test_vector_and_scalar_kernels_agree_bit_for_bit():
+    """A view whose rows start off a 16-byte boundary takes the scalar kernel; the same
+    values in an aligned tensor take the vector kernel.  Both round x1 c - x2 s once."""
+    for dtype in (torch.bfloat16, torch.float16, torch.float32):
+        for inter in (False, True):
+            ri = make_rotary_inputs(B=2, N=3, S=45, D=64, dtype=dtype, interleaved=inter, seed=21)
+            d = ri.to("cuda")
+            store = torch.zeros(2, 3, 45, 66, dtype=dtype, device="cuda")
+            xm = store[..., 1:65]                                       # misaligned rows
+            xm.copy_(d.x)
+            y_vec = sdpa.sdpa_rotary(d.x, d.cos, d.sin, d.position_ids, interleaved=inter)
+            y_sca = sdpa.sdpa_rotary(xm, d.cos, d.sin, d.position_ids, interleaved=inter)
+            assert sdpa.sdpa_query_status() == sdpa.SDPA_OK
+            iv = torch.int32 if dtype == torch.float32 else torch.int16
+            assert torch.equal(y_vec.view(iv), y_sca.contiguous().view(iv)), (dtype, inter)
+            check_rotated(y_sca, ri.x, oracle.rotary(ri.x, ri.cos, ri.sin, ri.position_ids, 0, inter), 64, inter)
 
 
 def test_position_outside_the_cache_is_reported_and_the_context_survives():
