@@ -149,10 +149,22 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-def source_digest() -> str:
-    h = hashlib.sha256()
+# Sources each kernel family is built from: a traffic figure stays valid while they hash
+# to the digest recorded with it.
+KERNEL_SOURCES = {
+    "prefill_tc": ("prefill_tc.cu", "prefill_tc.h", "tc_ptx.cuh", "common.cuh"),
+    "decode_splitkv": ("decode.cu", "internal.h", "common.cuh"),
+    "rotary": ("rotary.cu", "internal.h", "common.cuh"),
+    "qk_tc": ("qk.cu", "prefill_tc.h", "tc_ptx.cuh", "common.cuh"),
+}
+
+
+def source_digest(kernel: str) -> str:
+    fam = next((f for f in KERNEL_SOURCES if kernel.startswith(f)), None)
     csrc = os.path.join(ROOT, "scaled_dot_product_gb300", "csrc")
-    for n in sorted(os.listdir(csrc)):
+    names = KERNEL_SOURCES[fam] if fam else tuple(sorted(os.listdir(csrc)))
+    h = hashlib.sha256()
+    for n in names:
         h.update(n.encode())
         h.update(open(os.path.join(csrc, n), "rb").read())
     return h.hexdigest()[:16]
@@ -164,7 +176,7 @@ def ncu_traffic(kernel: str):
     if not os.path.exists(p):
         return None
     d = json.load(open(p)).get(kernel)
-    if not d or d.get("source_digest") != source_digest():
+    if not d or d.get("source_digest") != source_digest(kernel):
         return None
     return d.get("dram_bytes_per_launch")
 
@@ -289,7 +301,7 @@ def measure_rotary(steps: int, warmup: int, barrier, hbm: float):
     return {"workload": "rotary_bf16_b4_s4096_n32_d128_position_ids", "value": gbs, "unit": "GB/s",
             "ms_per_step": m, "kernel": "rotary", "gpu_launches": launches,
             "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
-                         "traffic": None}, "l2_flush": True}
+                         "traffic": ncu_traffic("rotary")}, "l2_flush": True}
 
 
 def metric_of(idx: int, case: Case, ms: float):
@@ -517,6 +529,7 @@ def main():
                 qkl.append({"workload": c.name + f"_qk_mode{mode}", "ms_per_step": m, "qk_extra_ms": extra_ms,
                             "qk_out_bytes": out_bytes, "qk_GBps_over_extra_time": gbs,
                             "frac_of_hbm": None if gbs is None else gbs / hbm,
+                            "traffic": ncu_traffic("qk_tc_bf16_h128") if mode == 0 else None,
                             "kernel": r["kernel"], "gpu_launches": r["launches"]})
                 del r
                 torch.cuda.empty_cache()
