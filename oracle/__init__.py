@@ -84,6 +84,9 @@ def lib():
         _lib.oracle_qk_rows.restype = ctypes.c_int
         _lib.oracle_qk_rows.argtypes = [ctypes.POINTER(_Params), ctypes.c_int32, ctypes.c_void_p,
                                         ctypes.c_int64, ctypes.c_void_p, ctypes.c_int]
+        _lib.oracle_attention_backward.restype = ctypes.c_int
+        _lib.oracle_attention_backward.argtypes = [ctypes.POINTER(_Params), ctypes.POINTER(_Tensor), ctypes.c_void_p,
+                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         _lib.oracle_present.restype = ctypes.c_int
         _lib.oracle_present.argtypes = [ctypes.c_int32] * 6 + [ctypes.POINTER(_Tensor)] * 2 + \
             [ctypes.c_void_p, ctypes.c_void_p]
@@ -218,6 +221,23 @@ def qk(pr: Problem, mode: int, nthreads: int = 0) -> np.ndarray:
     rows = np.stack(np.meshgrid(np.arange(B), np.arange(Nq), np.arange(S), indexing="ij"), -1)
     out, _ = qk_rows(pr, mode, rows.reshape(-1, 3), nthreads)
     return out.reshape(B, Nq, S, P + L)
+
+
+def backward(pr: Problem, dy: torch.Tensor, nthreads: int = 0):
+    """Gradients (dq, dk, dv) in float64 of the attention for the upstream gradient dy
+    (B, Nq, S, Hv): shapes (B, Nq, S, H), (B, Nkv, P+L, H), (B, Nkv, P+L, Hv)."""
+    keep: list = []
+    p = _params(pr, keep)
+    dyv = _view(dy, keep)
+    T = p.P + p.L
+    dq = np.zeros((p.B, p.Nq, p.S, p.H))
+    dk = np.zeros((p.B, p.Nkv, T, p.H))
+    dv = np.zeros((p.B, p.Nkv, T, p.Hv))
+    n = lib().oracle_attention_backward(ctypes.byref(p), ctypes.byref(dyv), dq.ctypes.data, dk.ctypes.data,
+                                        dv.ctypes.data, int(nthreads))
+    if n < 0:
+        raise ValueError(f"oracle rejected the problem (code {n})")
+    return dq, dk, dv
 
 
 def attention(pr: Problem, nthreads: int = 0) -> np.ndarray:

@@ -365,6 +365,115 @@ int oracle_qk_rows(const orc_params* p, int32_t mode, const int64_t* rows, int64
   return run_rows(p, mode, rows, nrows, out, nthreads);
 }
 
+/* ---- backward: the GroupQueryAttention gradient graph ("Custom operators", C++ API,
+ * RegisterCustomOperatorGradients).  Probabilities P from the forward's stage 3 (class
+ * Attention, mode 3); softmax backward dS = P * (dP - rowsum(P * dP)) with dP = dY V^T; the
+ * score scale replayed on dS; dQ = dS K, dK = dS^T Q and dV = P^T dY, the grouped query
+ * heads summed back onto their kv head.  Softcap has no place in that graph: rejected. ---- */
+
+typedef struct {
+  const orc_params* p;
+  const orc_tensor* dy;
+  double *dq, *dk, *dv;
+  int tid, nthreads;
+  int status;
+} bwd_arg;
+
+static void* bwd_worker(void* argp) {
+  bwd_arg* a = (bwd_arg*)argp;
+  const orc_params* p = a->p;
+  const int64_t T = (int64_t)p->P + p->L;
+  const int64_t group = p->Nq / p->Nkv;
+  row_scratch w;
+  w.q = (double*)malloc(sizeof(double) * (size_t)(p->H + 1));
+  w.krow = (double*)malloc(sizeof(double) * (size_t)(p->H + 1));
+  w.vrow = (double*)malloc(sizeof(double) * (size_t)(p->Hv + 1));
+  w.raw = (double*)malloc(sizeof(double) * (size_t)(T + 1));
+  w.nocap = (double*)malloc(sizeof(double) * (size_t)(T + 1));
+  w.s = (double*)malloc(sizeof(double) * (size_t)(T + 1));
+  w.alive = (char*)malloc((size_t)(T + 1));
+  double* prob = (double*)malloc(sizeof(double) * (size_t)(T + 1));
+  double* dp = (double*)malloc(sizeof(double) * (size_t)(T + 1));
+  double* dyrow = (double*)malloc(sizeof(double) * (size_t)(p->Hv + 1));
+  if (!w.q || !w.krow || !w.vrow || !w.raw || !w.nocap || !w.s || !w.alive || !prob || !dp || !dyrow) {
+    a->status = -2;
+  } else {
+    /* one (batch, kv head) per unit: every write of the unit lands in its own rows */
+    for (int64_t unit = a->tid; unit < (int64_t)p->B * p->Nkv; unit += a->nthreads) {
+      const int64_t b = unit / p->Nkv, kh = unit % p->Nkv;
+      for (int64_t h = kh * group; h < (kh + 1) * group; ++h)
+        for (int64_t i = 0; i < p->S; ++i) {
+          qk_row(p, 3, b, h, i, prob, &w);             /* P of the row; w->q holds q_i */
+          const int64_t yo = offset4(a->dy, b, h, i);
+          for (int64_t d = 0; d < p->Hv; ++d) dyrow[d] = oracle_to_double(a->dy->dtype, a->dy->data, yo + d);
+          double delta = 0.0;                           /* rowsum(P * dP) */
+          for (int64_t j = 0; j < T; ++j) {
+            dp[j] = 0.0;
+            if (prob[j] == 0.0) continue;
+            kv_row(p, 1, b, kh, j, w.vrow);
+            double acc = 0.0;
+            for (int64_t d = 0; d < p->Hv; ++d) acc += dyrow[d] * w.vrow[d];
+            dp[j] = acc;
+            delta += prob[j] * acc;
+          }
+          double* dqr = a->dq + ((b * p->Nq + h) * p->S + i) * p->H;
+          for (int64_t j = 0; j < T; ++j) {
+            if (prob[j] == 0.0) continue;
+            const double ds = prob[j] * (dp[j] - delta) * p->scale;
+            kv_row(p, 0, b, kh, j, w.krow);
+            double* dkr = a->dk + ((b * p->Nkv + kh) * T + j) * p->H;
+            double* dvr = a->dv + ((b * p->Nkv + kh) * T + j) * p->Hv;
+            for (int64_t d = 0; d < p->H; ++d) {
+              dqr[d] += ds * w.krow[d];
+              dkr[d] += ds * w.q[d];
+            }
+            for (int64_t d = 0; d < p->Hv; ++d) dvr[d] += prob[j] * dyrow[d];
+          }
+        }
+    }
+  }
+  free(w.q); free(w.krow); free(w.vrow); free(w.raw); free(w.nocap); free(w.s); free(w.alive);
+  free(prob); free(dp); free(dyrow);
+  return NULL;
+}
+
+int oracle_attention_backward(const orc_params* p, const orc_tensor* dy, double* dq, double* dk, double* dv,
+                              int nthreads) {
+  if (!p || !dy || !dy->data || !dq || !dk || !dv) return -1;
+  if (p->Nkv <= 0 || p->Nq % p->Nkv != 0) return -1;
+  if (p->window > 0 && p->causal == ORC_CAUSAL_NONE) return -1;
+  if (p->len_kind != ORC_LEN_NONE && !p->lens) return -1;
+  if (p->softcap > 0.0) return -1;
+  const int64_t T = (int64_t)p->P + p->L;
+  memset(dq, 0, sizeof(double) * (size_t)((int64_t)p->B * p->Nq * p->S * p->H));
+  memset(dk, 0, sizeof(double) * (size_t)((int64_t)p->B * p->Nkv * T * p->H));
+  memset(dv, 0, sizeof(double) * (size_t)((int64_t)p->B * p->Nkv * T * p->Hv));
+  if (nthreads <= 0) nthreads = (int)sysconf(_SC_NPROCESSORS_ONLN);
+  const int64_t units = (int64_t)p->B * p->Nkv;
+  if (nthreads < 1) nthreads = 1;
+  if ((int64_t)nthreads > units) nthreads = units > 0 ? (int)units : 1;
+  pthread_t* th = (pthread_t*)malloc(sizeof(pthread_t) * (size_t)nthreads);
+  bwd_arg* args = (bwd_arg*)malloc(sizeof(bwd_arg) * (size_t)nthreads);
+  if (!th || !args) { free(th); free(args); return -2; }
+  int started = 0;
+  for (int t = 0; t < nthreads; ++t) {
+    args[t] = (bwd_arg){p, dy, dq, dk, dv, t, nthreads, 0};
+    if (pthread_create(&th[t], NULL, bwd_worker, &args[t]) != 0) break;
+    ++started;
+  }
+  int status = 0;
+  for (int t = 0; t < started; ++t) pthread_join(th[t], NULL);
+  for (int t = 0; t < started; ++t) if (args[t].status) status = args[t].status;
+  for (int t = started; t < nthreads; ++t) {
+    bwd_arg a1 = {p, dy, dq, dk, dv, t, nthreads, 0};
+    bwd_worker(&a1);
+    if (a1.status) status = a1.status;
+  }
+  free(th);
+  free(args);
+  return status ? status : nthreads;
+}
+
 /* ---- rounding of a double array to an element type (once, to nearest even) ---- */
 
 int oracle_round_array(int32_t dtype, const double* in, int64_t n, void* out) {

@@ -91,6 +91,15 @@ int oracle_attention_rows(const orc_params* p, const int64_t* rows, int64_t nrow
 int oracle_qk_rows(const orc_params* p, int32_t mode, const int64_t* rows, int64_t nrows, double* out,
                    int nthreads);
 
+/* Backward of the attention (the GroupQueryAttention gradient graph): given dY (B, Nq, S,
+ * Hv), writes dQ (B, Nq, S, H), dK (B, Nkv, P+L, H) and dV (B, Nkv, P+L, Hv) as contiguous
+ * doubles (gradients with respect to the rows the scores see: past rows first).
+ * P = the stage-3 probabilities; dS = P (dY V^T - rowsum(P dY V^T)) * scale; dQ = dS K;
+ * dK = dS^T Q and dV = P^T dY summed over the query heads of each kv head.  Softcap > 0 is
+ * rejected.  Returns the number of threads used, or a negative value on a bad argument. */
+int oracle_attention_backward(const orc_params* p, const orc_tensor* dy, double* dq, double* dk, double* dv,
+                              int nthreads);
+
 /* Present tensor (B, N, P+L, D), contiguous, in dtype: past positions followed by the new
  * ones (new + bias, rounded once to dtype, when bias is given). */
 int oracle_present(int32_t dtype, int32_t B, int32_t N, int32_t P, int32_t L, int32_t D,

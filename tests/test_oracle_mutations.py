@@ -25,6 +25,12 @@ MUTATIONS = {
     "qk_mode1_keeps_excluded_scores": ("w->nocap[j] = excluded ? -INFINITY : nocap;", "w->nocap[j] = nocap;"),
     "qk_mode2_before_softcap": ("out[j] = w->s[j]; return;", "out[j] = w->nocap[j]; return;"),
     "qk_mode3_unnormalised": ("exp(w->s[j] - m) / l : 0.0;", "exp(w->s[j] - m) : 0.0;"),
+    "bwd_delta_dropped": ("const double ds = prob[j] * (dp[j] - delta) * p->scale;",
+                          "const double ds = prob[j] * dp[j] * p->scale;"),
+    "bwd_scale_dropped": ("const double ds = prob[j] * (dp[j] - delta) * p->scale;",
+                          "const double ds = prob[j] * (dp[j] - delta);"),
+    "bwd_dk_from_probabilities": ("dkr[d] += ds * w.q[d];", "dkr[d] += prob[j] * w.q[d];"),
+    "bwd_dv_from_score_gradient": ("dvr[d] += prob[j] * dyrow[d];", "dvr[d] += ds * dyrow[d];"),
     "lower_right_shift": ("pos = valid_total - p->S + i;", "pos = valid_total - p->S + i + 1;"),
     "f16_exponent_bias": ("e - 25);", "e - 24);"),
     "past_not_first": ("if (j < p->P) {", "if (j >= p->L) {"),

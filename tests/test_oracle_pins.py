@@ -609,3 +609,106 @@ def test_qk_fully_excluded_row_and_filter_values():
     np.testing.assert_allclose(m1[0, :, :, 4:], raw[0, :, :, 4:] - 50.0, atol=1e-12)
     np.testing.assert_array_equal(m1[0, :, :, :4], raw[0, :, :, :4])
     np.testing.assert_array_equal(m1[1], raw[1])
+
+
+# ---------------------------------------------------------------- backward (GroupQueryAttention gradient graph)
+
+def _torch_grads(q, k, v, dy, **kw):
+    q, k, v = (t.clone().double().requires_grad_(True) for t in (q, k, v))
+    y = F.scaled_dot_product_attention(q, k, v, **kw)
+    y.backward(dy.double())
+    return q.grad.numpy(), k.grad.numpy(), v.grad.numpy()
+
+
+@pytest.mark.parametrize("kind", ["plain", "gqa", "causal", "float_mask", "bool_mask", "scale"])
+def test_backward_equals_torch_autograd(kind):
+    B, Nq, Nkv, S, T, H, Hv = 2, 4, 4, 5, 7, 8, 6
+    if kind == "gqa":
+        Nkv = 2
+    q, k, v = rnd(B, Nq, S, H, seed=101), rnd(B, Nkv, T, H, seed=102), rnd(B, Nkv, T, Hv, seed=103)
+    dy = rnd(B, Nq, S, Hv, seed=104)
+    kw, tkw = {}, {}
+    if kind == "gqa":
+        tkw["enable_gqa"] = True
+    if kind == "causal":
+        kw["causal"], tkw["is_causal"] = oracle.CAUSAL_UPPER_LEFT, True
+    if kind == "float_mask":
+        m = rnd(B, Nq, S, T, seed=105)
+        kw["add_mask"], tkw["attn_mask"] = m, m
+    if kind == "bool_mask":
+        keep = (rnd(B, 1, S, T, seed=106) > -0.5)
+        keep[..., 0] = True                                   # every row keeps a key
+        kw["keep_mask"], kw["keep_kind"] = keep.to(torch.uint8).expand(B, Nq, S, T), oracle.KEEP_BOOL
+        tkw["attn_mask"] = keep
+    if kind == "scale":
+        kw["scale"], tkw["scale"] = 0.41, 0.41
+    dq, dk, dv = oracle.backward(Problem(q=q, k=k, v=v, **kw), dy)
+    wq, wk, wv = _torch_grads(q, k, v, dy, **tkw)
+    for got, want in ((dq, wq), (dk, wk), (dv, wv)):
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+def test_backward_with_window_sink_and_lower_right_past_equals_autograd_of_the_definition():
+    """A torch float64 forward written from the definition (the sink as an extra logit
+    column with no value), differentiated by autograd."""
+    B, Nq, Nkv, S, L, P, H = 1, 4, 2, 4, 4, 3, 8
+    q = rnd(B, Nq, S, H, seed=110)
+    k, v = rnd(B, Nkv, L, H, seed=111), rnd(B, Nkv, L, H, seed=112)
+    pk, pv = rnd(B, Nkv, P, H, seed=113), rnd(B, Nkv, P, H, seed=114)
+    sink, dy = rnd(Nq, seed=115), rnd(B, Nq, S, H, seed=116)
+    dq, dk, dv = oracle.backward(Problem(q=q, k=k, v=v, past_k=pk, past_v=pv, causal=oracle.CAUSAL_LOWER_RIGHT,
+                                         window=3, head_sink=sink), dy)
+    qt = q.clone().requires_grad_(True)
+    kt = torch.cat([pk, k], 2).clone().requires_grad_(True)
+    vt = torch.cat([pv, v], 2).clone().requires_grad_(True)
+    T = P + L
+    ke, ve = kt.repeat_interleave(Nq // Nkv, 1), vt.repeat_interleave(Nq // Nkv, 1)
+    s = torch.matmul(qt, ke.transpose(-1, -2)) / math.sqrt(H)
+    pos = (T - S + torch.arange(S)).view(S, 1)
+    j = torch.arange(T).view(1, T)
+    s = s.masked_fill((j > pos) | (j < pos - 3 + 1), -math.inf)
+    logits = torch.cat([s, sink.view(1, Nq, 1, 1).expand(B, Nq, S, 1)], -1)
+    prob = torch.softmax(logits, -1)[..., :T]
+    (torch.matmul(prob, ve) * dy).sum().backward()
+    np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dk, kt.grad.numpy(), atol=1e-12)
+    np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-12)
+
+
+def test_backward_matches_central_differences_of_the_forward():
+    """d(sum dY * Y)/dx from the oracle backward against central differences of the oracle
+    forward, with GQA, an additive mask, key lengths (filter), a boolean mask and a sink."""
+    B, Nq, Nkv, S, L, H = 1, 2, 1, 3, 5, 4
+    q, k, v = rnd(B, Nq, S, H, seed=120), rnd(B, Nkv, L, H, seed=121), rnd(B, Nkv, L, H, seed=122)
+    mask, sink, dy = rnd(B, Nq, S, L, seed=123), rnd(Nq, seed=124), rnd(B, Nq, S, H, seed=125)
+    keep = torch.ones(B, Nq, S, L, dtype=torch.uint8)
+    keep[0, 1, 2, 1] = 0
+    kw = dict(add_mask=mask, head_sink=sink, keep_mask=keep, keep_kind=oracle.KEEP_BOOL,
+              len_kind=oracle.LEN_KEYLEN_I32, lens=torch.tensor([4], dtype=torch.int32), mask_filter_value=-3.0)
+    dq, dk, dv = oracle.backward(Problem(q=q, k=k, v=v, **kw), dy)
+
+    def loss(q_, k_, v_):
+        return float((oracle.attention(Problem(q=q_, k=k_, v=v_, **kw)) * dy.numpy()).sum())
+
+    h = 1e-6
+    for name, t, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+        for idx in [(0, 0, 0, 0), (0, 0, 1, 2), (0, t.shape[1] - 1, t.shape[2] - 1, t.shape[3] - 1), (0, 0, 2, 3)]:
+            tp, tm = t.clone(), t.clone()
+            tp[idx] += h
+            tm[idx] -= h
+            args_p = {"q": q, "k": k, "v": v}
+            args_m = dict(args_p)
+            args_p[name], args_m[name] = tp, tm
+            fd = (loss(args_p["q"], args_p["k"], args_p["v"]) - loss(args_m["q"], args_m["k"], args_m["v"])) / (2 * h)
+            assert abs(fd - g[idx]) < 1e-7, (name, idx, fd, g[idx])
+
+
+def test_backward_of_rows_with_nothing_admitted_is_zero_and_softcap_is_rejected():
+    q, k, v = rnd(1, 2, 4, 8, seed=130), rnd(1, 2, 6, 8, seed=131), rnd(1, 2, 6, 8, seed=132)
+    dy = rnd(1, 2, 4, 8, seed=133)
+    keep = torch.ones(1, 2, 4, 6, dtype=torch.uint8)
+    keep[0, 0, 1] = 0
+    dq, dk, dv = oracle.backward(Problem(q=q, k=k, v=v, keep_mask=keep, keep_kind=oracle.KEEP_BOOL), dy)
+    np.testing.assert_array_equal(dq[0, 0, 1], 0.0)
+    with pytest.raises(ValueError):
+        oracle.backward(Problem(q=q, k=k, v=v, softcap=5.0), dy)
