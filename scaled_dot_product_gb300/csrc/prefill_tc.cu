@@ -22,6 +22,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <cmath>
 #include <cstdlib>
 #include <mutex>
 #include <type_traits>
@@ -39,21 +40,21 @@ using namespace ptx;
 
 constexpr int kBM = 128;        // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;        // keys per tile
-constexpr int kSplit = 1;                         // softmax threads per query row
-constexpr int kHalf = kBN / kSplit;               // score columns per softmax thread
-
-// CTA shape for QT 128-row query tiles per CTA (1: two CTAs share an SM; 2: one CTA).
-template <int QT>
+// CTA shape for QT 128-row query tiles per CTA (1: two CTAs share an SM; 2: one CTA) and
+// SPLIT softmax threads per query row (each owns 128 / SPLIT score columns of a key tile).
+template <int QT, int SPLIT>
 struct Layout {
-  static constexpr int kQT = QT;
-  static constexpr int kSmxThreads = 128 * QT * kSplit;   // softmax warpgroups
+  static constexpr int kSmxThreads = 128 * QT * SPLIT;    // softmax warpgroups
   static constexpr int kThreads = 128 + kSmxThreads;      // + 4 control warps
   static constexpr int kMinBlocks = (QT == 1) ? 2 : 1;
   // Register split (setmaxnreg): the control warpgroup shrinks to kCtlRegs, the softmax
   // warpgroups grow to kSmxRegs.  The sum must not exceed what the block was launched with
   // (kThreads x the kernel's register count), which the host checks before every launch.
   static constexpr int kLaunchRegs = (65536 / (kThreads * kMinBlocks)) & ~7;
-  static constexpr int kCtlRegs = (QT == 1) ? 64 : 80;
+#ifndef SDPA_CTL_REGS_SMALL
+#define SDPA_CTL_REGS_SMALL 56
+#endif
+  static constexpr int kCtlRegs = (kLaunchRegs <= 96) ? SDPA_CTL_REGS_SMALL : ((QT == 1) ? 64 : 80);
   static constexpr int kSmxRegs = ((kLaunchRegs * kThreads - kCtlRegs * 128) / kSmxThreads) & ~7;
   static_assert(kSmxRegs <= 256 && kSmxRegs >= kLaunchRegs, "register split");
   static_assert(kCtlRegs * 128 + kSmxRegs * kSmxThreads <= kLaunchRegs * kThreads, "register split");
@@ -63,6 +64,10 @@ constexpr float kRescaleThreshold = 8.f;   // log2 units
 // alternating Taylor series' error is below its next term, 17/315 u^7 <= 3.3e-6.
 constexpr float kTanhPolyLimit = 0.25f;
 constexpr float kTanhA1 = -1.f / 3.f, kTanhA2 = 2.f / 15.f;
+
+// Softcap with a fixed maximum (bf16 only): tanh(u) on |u| <= kTanhPolyLimit by the odd cubic
+// minimax fit a1 u + a3 u^3 (Remez exchange on [0, 0.25]; maximum error 7.8e-6).
+constexpr float kTanhMM1 = 0.99984343f, kTanhMM3 = -0.32319898f;
 
 __device__ __forceinline__ float tanh_poly(float u) {
   const float z = u * u;
@@ -97,6 +102,8 @@ struct TcArgs {
   int B, Nq, Nkv, S, T, group, nunits;
   float scale, scale_log2, cap_in, cap_out_log2;   // cap_* used when softcap > 0
   int has_softcap;
+  int cap_fixed;                                    // bf16 softcap: fixed row maximum (below)
+  float fx_a, fx_b, fx_lim;                         // cubic coefficients on raw q.k, its range
   int causal, window, len_kind;
   const void* lens;
   int generic;                                      // per-element rules beyond the structural ones
@@ -238,16 +245,21 @@ __device__ __noinline__ float generic_score(const Rules& r, const RowCtx& ctx, f
   return apply_rules(r, ctx, s_nat, b, h, i, j);
 }
 
-// Score-rule paths, fixed per launch.
-enum RuleMode { kPlain = 0, kAddMask = 1, kGeneric = 2 };
+// Score-rule paths, fixed per launch.  kCapFixed: interval rules with softcap on bf16.  The
+// capped logits lie in [-c, c], so the softmax uses the fixed maximum c (log2 domain: c log2 e)
+// instead of a running one: no row maximum, no rescale of the accumulator.  Every weight is
+// then at least 2^(-2 c log2 e), a normal number in fp32 and bf16 for c <= 40.
+enum RuleMode { kPlain = 0, kAddMask = 1, kGeneric = 2, kCapFixed = 3 };
 
-template <int H, bool kBF16, int kMode, int QT>
-__global__ void __launch_bounds__(Layout<QT>::kThreads, Layout<QT>::kMinBlocks)
+template <int H, bool kBF16, int kMode, int QT, int SPLIT>
+__global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>::kMinBlocks)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const TcArgs a) {
   using C = Cfg<H, QT>;
-  using Lay = Layout<QT>;
+  using Lay = Layout<QT, SPLIT>;
   constexpr int kQT = QT;
+  constexpr int kSplit = SPLIT;                     // softmax threads per query row
+  constexpr int kHalf = kBN / kSplit;               // score columns per softmax thread
   constexpr int kSmxThreads = Lay::kSmxThreads;
   using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
   extern __shared__ unsigned char smem_raw[];
@@ -510,6 +522,10 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, Layout<QT>::kMinBlocks)
     // generic mode produces log2-domain scores already
     const float kfac = (kMode == kPlain) ? (a.has_softcap ? a.cap_out_log2 : a.scale_log2)
                                          : (kMode == kAddMask ? kLog2e : 1.f);
+    // kCapFixed: the fixed maximum (the cap, or the sink logit when that is larger)
+    float m_fixed = a.cap_out_log2;
+    if (kMode == kCapFixed && a.head_sink)
+      m_fixed = fmaxf(m_fixed, Elem<T>::to_f32(reinterpret_cast<const T*>(a.head_sink)[qh]) * kLog2e);
     bool ok = true;
 
     if (n_tiles > 0 && a.q_bias) {
@@ -542,7 +558,7 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, Layout<QT>::kMinBlocks)
       mbar_arrive(b_qready);
     }
 
-    float m_use = -INFINITY, l = 0.f;
+    float m_use = (kMode == kCapFixed) ? m_fixed : -INFINITY, l = 0.f;
     for (int j = 0; j < n_tiles && ok; ++j) {
       uint32_t mraw[kMode == kAddMask ? kHalf / 2 : 1];
       if constexpr (kMode == kAddMask) {
@@ -570,7 +586,51 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, Layout<QT>::kMinBlocks)
       const int key0 = (kv_t0 + j) * kBN + kHalf * hh;
       bool have_mx = false;       // set when the transform already produced this half's max
       float mx_own = -INFINITY;
-      if constexpr (kMode == kPlain) {
+      bool weights = false;       // kCapFixed: s already holds the weights p
+      if constexpr (kMode == kCapFixed) {
+        // s = raw q.k; the exponent c log2e tanh(s scale / c) - m, from the cubic when every
+        // |s| of the segment is in its range (eight chains of three-input max of |s|)
+        float am8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) am8[k] = fmaxf(fabsf(s[k]), fabsf(s[k + 8]));
+#pragma unroll
+        for (int e = 16; e < kHalf; e += 16)
+#pragma unroll
+          for (int k = 0; k < 8; ++k) am8[k] = fmax3(am8[k], fabsf(s[e + k]), fabsf(s[e + 8 + k]));
+        const float amax = fmax3(fmax3(am8[0], am8[1], am8[2]), fmax3(am8[3], am8[4], am8[5]), fmaxf(am8[6], am8[7]));
+        const float negm = -m_use;
+        const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
+        if (amax <= a.fx_lim && full) {
+          // every key admitted: exponent and weight in one pass, in place
+          const f2_t ca = f2_pack(a.fx_a, a.fx_a), cb = f2_pack(a.fx_b, a.fx_b), nm2 = f2_pack(negm, negm);
+#pragma unroll
+          for (int e = 0; e < kHalf; e += 2) {
+            const f2_t x2 = f2_pack(s[e], s[e + 1]);
+            const f2_t tt = f2_fma(f2_mul(x2, x2), cb, ca);
+            float z0, z1;
+            f2_unpack(f2_fma(x2, tt, nm2), z0, z1);
+            s[e] = ex2_approx(z0);
+            s[e + 1] = ex2_approx(z1);
+          }
+          weights = true;
+        } else if (amax <= a.fx_lim) {
+          const f2_t ca = f2_pack(a.fx_a, a.fx_a), cb = f2_pack(a.fx_b, a.fx_b), nm2 = f2_pack(negm, negm);
+#pragma unroll
+          for (int e = 0; e < kHalf; e += 2) {
+            const f2_t x2 = f2_pack(s[e], s[e + 1]);
+            const f2_t tt = f2_fma(f2_mul(x2, x2), cb, ca);
+            f2_unpack(f2_fma(x2, tt, nm2), s[e], s[e + 1]);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < kHalf; ++e) s[e] = fmaf(a.cap_out_log2, tanh_approx(s[e] * a.cap_in), negm);
+        }
+        if (!full) {
+          const int elo = lo32 - key0, ehi = hi32 - key0;
+#pragma unroll
+          for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
+        }
+      } else if constexpr (kMode == kPlain) {
         const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
         if (a.has_softcap) {
           const f2_t cin = f2_pack(a.cap_in, a.cap_in);
@@ -655,7 +715,7 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, Layout<QT>::kMinBlocks)
       }
 
       // row maximum: this half (eight chains of three-input max), then the partner's half
-      if (!have_mx) {
+      if (kMode != kCapFixed && !have_mx) {
         float mx8[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) mx8[k] = fmax3(s[k], s[k + 8], -INFINITY);
@@ -674,26 +734,42 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, Layout<QT>::kMinBlocks)
 
       // move the running maximum only when it grows by more than 2^8 (both halves of a
       // row see the same maxima, so they take the same decision)
-      const float m_tile = mx * kfac;
-      const float m_new = fmaxf(m_use, m_tile);
-      const bool need = m_new > m_use + kRescaleThreshold;
+      bool need = false;
       float corr = 1.f;
-      if (need) {
-        corr = ex2_approx(m_use - m_new);
-        m_use = m_new;
+      if constexpr (kMode != kCapFixed) {
+        const float m_tile = mx * kfac;
+        const float m_new = fmaxf(m_use, m_tile);
+        need = m_new > m_use + kRescaleThreshold;
+        if (need) {
+          corr = ex2_approx(m_use - m_new);
+          m_use = m_new;
+        }
       }
-      // rows with nothing admitted yet get exponent -inf, hence p = 0
-      const float negm = (m_use == -INFINITY) ? -INFINITY : -m_use;
-      const f2_t kf2 = f2_pack(kfac, kfac), nm2 = f2_pack(negm, negm);
       f2_t acc2[4] = {f2_zero(), f2_zero(), f2_zero(), f2_zero()};
       uint32_t pw[kHalf / 2];
+      if constexpr (kMode == kCapFixed) {
+        // s holds the exponents (masked keys: -inf), or the weights already
+        if (!weights) {
 #pragma unroll
-      for (int e = 0; e < kHalf; e += 2) {
-        float z0, z1;
-        f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), kf2, nm2), z0, z1);
-        const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-        acc2[(e >> 1) & 3] = f2_add(acc2[(e >> 1) & 3], f2_pack(p0, p1));
-        pw[e >> 1] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+          for (int e = 0; e < kHalf; ++e) s[e] = ex2_approx(s[e]);
+        }
+#pragma unroll
+        for (int e = 0; e < kHalf; e += 2) {
+          acc2[(e >> 1) & 3] = f2_add(acc2[(e >> 1) & 3], f2_pack(s[e], s[e + 1]));
+          pw[e >> 1] = pack_bf16x2(s[e], s[e + 1]);
+        }
+      } else {
+        // rows with nothing admitted yet get exponent -inf, hence p = 0
+        const float negm = (m_use == -INFINITY) ? -INFINITY : -m_use;
+        const f2_t kf2 = f2_pack(kfac, kfac), nm2 = f2_pack(negm, negm);
+#pragma unroll
+        for (int e = 0; e < kHalf; e += 2) {
+          float z0, z1;
+          f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), kf2, nm2), z0, z1);
+          const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+          acc2[(e >> 1) & 3] = f2_add(acc2[(e >> 1) & 3], f2_pack(p0, p1));
+          pw[e >> 1] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
+        }
       }
       float r0, r1, r2, r3, r4, r5, r6, r7;
       f2_unpack(acc2[0], r0, r1);
@@ -709,7 +785,7 @@ __global__ void __launch_bounds__(Layout<QT>::kThreads, Layout<QT>::kMinBlocks)
           if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_odone(x), (j - 1) & 1, abortp, a.wait_ns)))) break;
           tc_fence_after();
         }
-        if (__any_sync(0xffffffffu, need)) {
+        if (kMode != kCapFixed && __any_sync(0xffffffffu, need)) {
           // rescale this thread's half of its row of the accumulator (factor 1 for rows
           // that kept their maximum)
           const f2_t c2 = f2_pack(corr, corr);
@@ -851,27 +927,27 @@ uint64_t wait_limit_ns() {
   return v;
 }
 
-template <int H, bool kBF16, int kMode, int QT>
+template <int H, bool kBF16, int kMode, int QT, int SPLIT>
 cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, TcArgs a,
                         int64_t units_per_qt_row, cudaStream_t st) {
   using C = Cfg<H, QT>;
-  using Lay = Layout<QT>;
+  using Lay = Layout<QT, SPLIT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, kBF16, kMode, QT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, kBF16, kMode, QT, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     C::kSmem);
     // the in-kernel register split assumes the block is launched with kLaunchRegs per
     // thread; with fewer, the softmax warps' request could never be met
     cudaFuncAttributes fa{};
-    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<H, kBF16, kMode, QT>);
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<H, kBF16, kMode, QT, SPLIT>);
     if (attr_err == cudaSuccess && fa.numRegs < Lay::kLaunchRegs) attr_err = cudaErrorLaunchOutOfResources;
   });
   if (attr_err != cudaSuccess) return attr_err;
   a.nunits = (a.S + QT * kBM - 1) / (QT * kBM);
   const int64_t units = units_per_qt_row * a.nunits;
   if (units > 0x7fffffff) return cudaErrorInvalidValue;
-  prefill_tc_kernel<H, kBF16, kMode, QT><<<(unsigned)units, Lay::kThreads, C::kSmem, st>>>(tq, tk, tv, a);
+  prefill_tc_kernel<H, kBF16, kMode, QT, SPLIT><<<(unsigned)units, Lay::kThreads, C::kSmem, st>>>(tq, tk, tv, a);
   count_launch(1);
   return cudaGetLastError();
 }
@@ -881,9 +957,11 @@ cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 template <int H, bool kBF16>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TcArgs& a,
                      int64_t heads_batches, cudaStream_t st) {
-  if (a.generic) return launch_mode<H, kBF16, kGeneric, 2>(tq, tk, tv, a, heads_batches, st);
-  if (a.add_fast) return launch_mode<H, kBF16, kAddMask, 2>(tq, tk, tv, a, heads_batches, st);
-  return launch_mode<H, kBF16, kPlain, 1>(tq, tk, tv, a, heads_batches, st);
+  if (a.generic) return launch_mode<H, kBF16, kGeneric, 2, 1>(tq, tk, tv, a, heads_batches, st);
+  if (a.add_fast) return launch_mode<H, kBF16, kAddMask, 2, 1>(tq, tk, tv, a, heads_batches, st);
+  if constexpr (kBF16)
+    if (a.cap_fixed) return launch_mode<H, kBF16, kCapFixed, 1, 1>(tq, tk, tv, a, heads_batches, st);
+  return launch_mode<H, kBF16, kPlain, 1, 1>(tq, tk, tv, a, heads_batches, st);
 }
 
 }  // namespace
@@ -925,6 +1003,13 @@ cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, 
   a.has_softcap = p.r.softcap > 0.f;
   a.cap_in = a.has_softcap ? p.scale / p.r.softcap : 0.f;
   a.cap_out_log2 = a.has_softcap ? p.r.softcap * kLog2e : 0.f;
+  if (a.has_softcap) {
+    // exponent = x (A + B x^2) - m on the raw product x = q.k, valid for |x scale / c| <= 0.25
+    const double cin = (double)p.scale / p.r.softcap, K = (double)p.r.softcap * kLog2e;
+    a.fx_a = (float)(kTanhMM1 * cin * K);
+    a.fx_b = (float)(kTanhMM3 * cin * cin * cin * K);
+    a.fx_lim = (float)(kTanhPolyLimit / std::fabs(cin));
+  }
   a.causal = p.r.causal;
   a.window = (int)p.r.window;
   a.len_kind = p.r.len_kind;
@@ -942,6 +1027,7 @@ cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, 
     a.add_vec = (int)(g & (~g + 1));   // lowest set bit
     if (a.add_vec > 16) a.add_vec = 16;
   }
+  a.cap_fixed = dt == SDPA_BF16 && a.has_softcap && p.r.softcap <= 40.f && !a.generic && !a.add_fast;
   a.r = p.r;
   a.y = const_cast<void*>(p.y.p);
   a.y_sb = p.y.sb; a.y_sh = p.y.sh; a.y_ss = p.y.ss;

@@ -218,3 +218,28 @@ def _sample_rows(case: Case, n: int, seed: int) -> np.ndarray:
 def test_workload_full_size_sampled(idx, op):
     case = workload(idx)
     run_and_compare(case, op, rows=_sample_rows(case, 96, 100 + idx))
+
+
+# ----------------------------------------------------------------- bf16 softcap, fixed maximum
+
+@pytest.mark.parametrize("H", [64, 128])
+@pytest.mark.parametrize("softcap,q_gain,sink", [
+    (30.0, 1.0, False),    # cubic tanh throughout
+    (30.0, 1.0, True),     # sink below the cap
+    (3.0, 1.0, True),      # arguments beyond the cubic's range: tanh on the special-function unit
+    (40.0, 12.0, False),   # logits near +-c: weights down to 2^(-2 c log2 e)
+    (8.0, 2.0, "big"),     # sink logit above the cap: it becomes the fixed maximum
+    (55.0, 3.0, False),    # cap above 40: the running-maximum path
+])
+def test_bf16_softcap_fixed_maximum(H, softcap, q_gain, sink):
+    """Softcap bounds every logit by +-c, so the bf16 kernel uses c (or a larger sink logit)
+    as the softmax maximum instead of a running one; results must not change."""
+    c = make_case(f"capfix_h{H}_c{softcap:g}", dtype=torch.bfloat16, B=2, Nq=4, Nkv=2, S=300, L=300, H=H,
+                  seed=40 + H, causal="upper_left", softcap=softcap, sink=bool(sink),
+                  len_kind="nonpad", len_range=(120, 300), q_layout="bsnh", kv_layout="bsnh")
+    if q_gain != 1.0:
+        c.q = (c.q.float() * q_gain).to(torch.bfloat16)
+    if sink == "big":
+        c.head_sink = (torch.arange(c.Nq, dtype=torch.float32) * 3.0 + softcap + 2.0).to(torch.bfloat16)
+    err, name = run_and_compare(c, "fwd")
+    assert name.startswith("prefill_tc"), name
