@@ -304,6 +304,47 @@ def measure_rotary(steps: int, warmup: int, barrier, hbm: float):
                          "traffic": ncu_traffic("rotary")}, "l2_flush": True}
 
 
+def backward_flops(case: Case) -> float:
+    """Algorithmic work of the backward (the GroupQueryAttention gradient graph): per admitted
+    (query, key) pair the score recompute Q K^T (2H), dP = dY V^T (2Hv), dQ = dS K (2H),
+    dK = dS^T Q (2H) and dV = P^T dY (2Hv), i.e. 2.5 times the forward's 2(H + Hv)."""
+    return float(admitted_pairs_per_row(case).sum()) * case.Nq * 2.0 * (3 * case.H + 2 * case.Hv)
+
+
+def measure_backward(idx: int, steps: int, warmup: int, barrier, tfl, tfl_src):
+    """Backward (sdpa_attn_bwd) on a workload: inputs and dY resident, dQ / dK / dV written
+    every step; L2 flushed between timed steps."""
+    from scaled_dot_product_gb300 import sdpa
+    from scaled_dot_product_gb300.workloads import as4d, draw_dy
+    case_cpu = workload(idx)
+    case = case_cpu.to("cuda")
+    q, k, v = case.views()
+    dy = as4d(draw_dy(case_cpu, seed=3000 + idx).to("cuda"), case.q_layout, case.Nq)
+    kw = sdpa.case_kwargs(case)
+    dq = torch.empty(case.B, case.Nq, case.S, case.H, dtype=case.dtype, device="cuda")
+    dk = torch.empty(case.B, case.Nkv, case.T, case.H, dtype=case.dtype, device="cuda")
+    dv = torch.empty(case.B, case.Nkv, case.T, case.Hv, dtype=case.dtype, device="cuda")
+    params, keep = sdpa.make_params(q, k, v, **kw)
+    ws = torch.empty(sdpa.sdpa_workspace_size(params, sdpa.SDPA_OP_BWD), dtype=torch.uint8, device="cuda")
+    run = lambda: sdpa.sdpa_attn_bwd(q, k, v, dy, dq=dq, dk=dk, dv=dv, workspace=ws, **kw)
+    run()
+    torch.cuda.synchronize()
+    kernel = sdpa.sdpa_last_kernel_name()
+    n0 = sdpa.sdpa_launch_count()
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        ms, _ = time_device(run, steps, warmup, flush, barrier)
+    launches = sdpa.sdpa_launch_count() - n0
+    m = statistics.mean(ms)
+    tf = backward_flops(case_cpu) / (m * 1e-3) / 1e12
+    return {"workload": case_cpu.name + "_backward", "value": tf, "unit": "TFLOP/s", "ms_per_step": m,
+            "work_per_step": f"{backward_flops(case_cpu):.4g} flop (2.5x the forward's)",
+            "kernel": kernel, "gpu_launches": launches, "launches_per_step": launches // max(1, steps + warmup),
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": tfl, "unit": "TFLOP/s", "frac": tf / tfl,
+                         "peak_source": f"{tfl_src} bf16 dense burst", "traffic": ncu_traffic(kernel)},
+            "l2_flush": True, "clocks": clk.summary()}
+
+
 def metric_of(idx: int, case: Case, ms: float):
     if is_decode(idx):
         return decode_bytes(case) / (ms * 1e-3) / 1e9, "GB/s"
@@ -409,6 +450,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end measurement")
     ap.add_argument("--batch", type=int, default=None,
                     help="override the batch size of the headline workload (profiling captures only)")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="measure only the backward on the GQA workload (profiling captures)")
     ap.add_argument("--ref-seconds", type=float, default=150.0,
                     help="total CPU time budget of the reference (oracle) arm")
     a = ap.parse_args()
@@ -456,6 +499,9 @@ def main():
         barrier()
     hbm, tfl, tfl_sus, src = peaks()
 
+    if a.backward_only:
+        print(json.dumps(measure_backward(3, a.steps, warmup, barrier, tfl, src)))
+        return
     res = measure_native(idx, a.steps, warmup, barrier, with_e2e=not a.no_e2e, batch=a.batch)
     case = res["case"]
     ms = statistics.mean(res["ms"])
@@ -515,6 +561,9 @@ def main():
             del r
             torch.cuda.empty_cache()
         line["rotary"] = nxt
+        # the backward (GroupQueryAttention gradient graph) on the windowed GQA workload
+        line["backward"] = [measure_backward(3, max(5, min(a.steps // 2, 100)), warmup, barrier, tfl, src)]
+        torch.cuda.empty_cache()
         # the auxiliary qk output (qk_matmul_output_mode 0 and 3) on the GQA prefill: the
         # output write is the added work; GB/s counts its bytes over the added time
         if idx == 2:

@@ -169,6 +169,7 @@ typedef struct {
 /* Which entry point a workspace query is for. */
 #define SDPA_OP_FWD    0
 #define SDPA_OP_DECODE 1
+#define SDPA_OP_BWD    2
 
 /* Prefill / general forward.  Writes y (and present_k/present_v when given).
  * workspace: device scratch of at least sdpa_workspace_size(p, SDPA_OP_FWD) bytes
@@ -209,13 +210,34 @@ SDPA_API int sdpa_attn_decode(const sdpa_params* p, void* workspace, size_t work
  *    order on one stream. */
 SDPA_API int sdpa_attn_decode_static(const sdpa_params* p, sdpa_stream_t stream);
 
-/* Bytes of device workspace the entry point `op` (SDPA_OP_FWD / SDPA_OP_DECODE) needs for
+/* Backward of the attention: the gradient graph of onnx-light-cpu "Custom operators" (C++
+ * API, RegisterCustomOperatorGradients, GroupQueryAttention gradient).  With P the stage-3
+ * probabilities of the forward (class Attention, qk_matmul_output_mode 3, sink in the
+ * denominator):
+ *     dP = dY V^T,  dS = P (dP - rowsum(P dP)) scale,  dQ = dS K,  dK = dS^T Q,  dV = P^T dY,
+ * the query heads of a group summed onto their kv head, every output rounded once to dtype.
+ * p describes the forward problem exactly as for sdpa_attn_fwd (p->y may be absent and is not
+ * written).  dy: (B, Nq, S, Hv) upstream gradient; outputs dq (B, Nq, S, H), dk (B, Nkv, L, H),
+ * dv (B, Nkv, L, Hv), all views of dtype elements, written in full (zeros where no score
+ * depends on them).  workspace: sdpa_workspace_size(p, SDPA_OP_BWD) bytes (two fp32 values per
+ * query row), 256-byte aligned.
+ * Subset: float16 / bfloat16, H == Hv in {64, 128}, P == 0, no projection biases, no rotary,
+ * no qk output, no present outputs; rules: causal (either alignment), window, nonpad_kv_seqlen
+ * or seqlens_k lengths, head_sink.  softcap > 0 returns SDPA_ERR_UNSUPPORTED (the gradient
+ * graph has no softcap), as do float / bool / filter masks and key-padding lengths.
+ * Alignment and aliasing rules as for sdpa_attn_fwd; outputs overlap no input. */
+SDPA_API int sdpa_attn_bwd(const sdpa_params* p, sdpa_view dy, sdpa_view dq, sdpa_view dk, sdpa_view dv,
+                           void* workspace, size_t workspace_bytes, sdpa_stream_t stream);
+
+/* Bytes of device workspace the entry point `op` (SDPA_OP_FWD / SDPA_OP_DECODE / SDPA_OP_BWD) needs for
  * these parameters; 0 when none.  Pure host function (no CUDA call); returns 0 and sets
  * sdpa_last_error() when the parameters are invalid. */
 SDPA_API size_t sdpa_workspace_size(const sdpa_params* p, int op);
 
-/* Host-only validation of p for `op`, exactly as the entry points perform it before any
- * launch.  No CUDA call.  Returns SDPA_OK or the error code the entry point would return. */
+/* Host-only validation of p for `op` (SDPA_OP_FWD / SDPA_OP_DECODE / SDPA_OP_BWD), exactly as
+ * the entry points perform it before any launch (for SDPA_OP_BWD: the problem's parameters and
+ * the backward's subset; the gradient views are checked by sdpa_attn_bwd itself).  No CUDA
+ * call.  Returns SDPA_OK or the error code the entry point would return. */
 SDPA_API int sdpa_validate(const sdpa_params* p, int op);
 
 /* RotaryEmbedding (onnx-light "include_nn_kernels.h", class RotaryEmbedding): y = x with

@@ -106,7 +106,7 @@ int validate(const sdpa_params* p, int op, Problem* pr, Rot* rot = nullptr) {
   if (p->struct_size != (int32_t)sizeof(sdpa_params))
     return fail(SDPA_ERR_INVALID, "struct_size %d != sizeof(sdpa_params) %d", p->struct_size,
                 (int)sizeof(sdpa_params));
-  if (op != SDPA_OP_FWD && op != SDPA_OP_DECODE) return fail(SDPA_ERR_INVALID, "unknown op %d", op);
+  if (op != SDPA_OP_FWD && op != SDPA_OP_DECODE && op != SDPA_OP_BWD) return fail(SDPA_ERR_INVALID, "unknown op %d", op);
   const int dt = p->dtype;
   if (dt != SDPA_F32 && dt != SDPA_F16 && dt != SDPA_BF16) return fail(SDPA_ERR_INVALID, "dtype %d", dt);
   if (p->B < 0 || p->S < 0 || p->L < 0 || p->P < 0)
@@ -184,7 +184,7 @@ int validate(const sdpa_params* p, int op, Problem* pr, Rot* rot = nullptr) {
   if ((rc = check_view(p->past_v, "past_v", dt, p->B, p->Nkv, p->P, p->Hv, p->P > 0, false, &epv))) return rc;
   if ((rc = check_view(p->present_k, "present_k", dt, p->B, p->Nkv, T, p->H, false, false, &eprk))) return rc;
   if ((rc = check_view(p->present_v, "present_v", dt, p->B, p->Nkv, T, p->Hv, false, false, &eprv))) return rc;
-  if ((rc = check_view(p->y, "y", dt, p->B, p->Nq, p->S, p->Hv, true, false, &ey))) return rc;
+  if ((rc = check_view(p->y, "y", dt, p->B, p->Nq, p->S, p->Hv, op != SDPA_OP_BWD, false, &ey))) return rc;
   Extent eqk;
   if ((rc = check_view(p->qk_out, "qk_out", SDPA_F32, p->B, p->Nq, p->S, T, false, false, &eqk))) return rc;
   const int mdt = p->add_mask.data ? p->add_mask_dtype : SDPA_F32;
@@ -283,6 +283,31 @@ size_t fwd_workspace(const Problem& r, sdpa_dtype dt) {
 
 size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
+// The backward's subset: the GroupQueryAttention gradient graph has no softcap, and this
+// library's kernels take 16-bit types, H == Hv in {64, 128}, no past rows, no projection
+// biases, no rotary step and the interval rules only (causal, window, nonpad / seqlens_k
+// lengths) plus the sink.
+int bwd_check(const sdpa_params* p, const Problem& r, const Rot& rot) {
+  const sdpa_dtype dt = (sdpa_dtype)p->dtype;
+  if (p->softcap > 0.f) return fail(SDPA_ERR_UNSUPPORTED, "the backward has no softcap derivative");
+  if (dt == SDPA_F32) return fail(SDPA_ERR_UNSUPPORTED, "backward: float16 / bfloat16 only");
+  if (!bwd_tc_supported(r, dt)) return fail(SDPA_ERR_UNSUPPORTED, "backward: H == Hv in {64, 128} only");
+  if (r.P > 0) return fail(SDPA_ERR_UNSUPPORTED, "backward: no past rows (P=%d)", r.P);
+  if (r.q_bias || r.k_bias || r.v_bias) return fail(SDPA_ERR_UNSUPPORTED, "backward: no projection biases");
+  if (rot.on) return fail(SDPA_ERR_UNSUPPORTED, "backward: no rotary step");
+  if (p->qk_out.data) return fail(SDPA_ERR_UNSUPPORTED, "backward: no qk output");
+  if (p->present_k.data) return fail(SDPA_ERR_INVALID, "backward: present outputs are not written");
+  if (p->add_mask.data || p->keep_kind != SDPA_KEEP_NONE || p->len_kind == SDPA_LEN_KEYLEN_I32)
+    return fail(SDPA_ERR_UNSUPPORTED, "backward: interval rules only (no float / bool / filter masks)");
+  if (!tc_same_axis_order(r.k, r.v, r.B, r.Nkv, r.T))
+    return fail(SDPA_ERR_UNSUPPORTED, "backward: k and v views must walk their axes in the same order");
+  return SDPA_OK;
+}
+
+size_t bwd_workspace(const Problem& r) {
+  return 2 * align256((size_t)r.B * r.Nq * (size_t)r.S * sizeof(float));
+}
+
 // Bytes of workspace for the rotated copies of Q and of the new K rows; 0 without rotary.
 size_t rot_workspace(const Problem& r, const Rot& rot, sdpa_dtype dt) {
   if (!rot.on) return 0;
@@ -359,7 +384,10 @@ extern "C" {
 
 int sdpa_validate(const sdpa_params* p, int op) {
   Problem r;
-  return validate(p, op, &r);
+  Rot rot;
+  const int rc = validate(p, op, &r, &rot);
+  if (rc || op != SDPA_OP_BWD) return rc;
+  return bwd_check(p, r, rot);
 }
 
 size_t sdpa_workspace_size(const sdpa_params* p, int op) {
@@ -369,6 +397,7 @@ size_t sdpa_workspace_size(const sdpa_params* p, int op) {
   const sdpa_dtype dt = (sdpa_dtype)p->dtype;
   const size_t pre = rot_workspace(r, rot, dt);
   if (op == SDPA_OP_DECODE) return pre + plan_decode(r.B, r.Nq, r.Nkv, r.S, r.T, r.Hv).ws_bytes;
+  if (op == SDPA_OP_BWD) return bwd_check(p, r, rot) == SDPA_OK ? bwd_workspace(r) : 0;
   return pre + fwd_workspace(after_rotary(r, rot, dt, nullptr), dt);
 }
 
@@ -575,15 +604,62 @@ int sdpa_rotary(sdpa_dtype dtype, int32_t B, int32_t N, int32_t S, int32_t D, sd
   return SDPA_OK;
 }
 
+int sdpa_attn_bwd(const sdpa_params* p, sdpa_view dy, sdpa_view dq, sdpa_view dk, sdpa_view dv, void* workspace,
+                  size_t workspace_bytes, sdpa_stream_t stream) {
+  Problem r;
+  Rot rot;
+  int rc = validate(p, SDPA_OP_BWD, &r, &rot);
+  if (rc) return rc;
+  if ((rc = bwd_check(p, r, rot))) return rc;
+  const int dt = p->dtype;
+  Extent edy, edq, edk, edv;
+  if ((rc = check_view(dy, "dy", dt, r.B, r.Nq, r.S, r.Hv, true, false, &edy))) return rc;
+  if ((rc = check_view(dq, "dq", dt, r.B, r.Nq, r.S, r.H, true, false, &edq))) return rc;
+  if ((rc = check_view(dk, "dk", dt, r.B, r.Nkv, r.T, r.H, true, false, &edk))) return rc;
+  if ((rc = check_view(dv, "dv", dt, r.B, r.Nkv, r.T, r.Hv, true, false, &edv))) return rc;
+  for (const sdpa_view* v : {&dy, &dq, &dk, &dv})
+    if ((rc = check_aligned_view(*v, v == &dy ? "dy" : v == &dq ? "dq" : v == &dk ? "dk" : "dv", dt))) return rc;
+  Extent eq, ek, ev;
+  check_view(p->q, "q", dt, r.B, r.Nq, r.S, r.H, true, false, &eq);
+  check_view(p->k, "k", dt, r.B, r.Nkv, r.L, r.H, true, false, &ek);
+  check_view(p->v, "v", dt, r.B, r.Nkv, r.L, r.Hv, true, false, &ev);
+  const Extent ins[] = {eq, ek, ev, edy, flat(p->head_sink, (size_t)r.Nq * esize(dt), "head_sink"),
+                        flat(p->lens, (size_t)r.B * (p->len_kind == SDPA_LEN_NONPAD_I64 ? 8 : 4), "lens")};
+  for (const Extent& o : {edq, edk, edv})
+    for (const Extent& in : ins)
+      if (overlap(o, in)) return fail(SDPA_ERR_ALIAS, "output %s overlaps input %s", o.name, in.name);
+  if (overlap(edq, edk) || overlap(edq, edv) || overlap(edk, edv))
+    return fail(SDPA_ERR_ALIAS, "outputs dq / dk / dv overlap");
+  const size_t need = bwd_workspace(r);
+  if (need && (!workspace || workspace_bytes < need))
+    return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
+  if (need && ((uintptr_t)workspace & 255u)) return fail(SDPA_ERR_ALIGNMENT, "workspace not 256-byte aligned");
+  if (need && overlap(flat(workspace, need, "workspace"), edq))
+    return fail(SDPA_ERR_ALIAS, "workspace overlaps dq");
+  g_error.clear();
+  if ((int64_t)r.B * r.Nq * r.S == 0 && (int64_t)r.B * r.Nkv * r.T == 0) return SDPA_OK;
+  auto cv = [](const sdpa_view& v) { return View{v.data, v.stride_b, v.stride_n, v.stride_s}; };
+  float* lse2 = reinterpret_cast<float*>(workspace);
+  float* delta = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + need / 2);
+  const char* name = "";
+  cudaError_t e = launch_bwd_tc(r, (sdpa_dtype)dt, cv(dy), cv(dq), cv(dk), cv(dv), lse2, delta,
+                                reinterpret_cast<cudaStream_t>(stream), &name);
+  if (e != cudaSuccess) return cuda_fail(e, "backward launch");
+  g_kernel = name;
+  return SDPA_OK;
+}
+
 int sdpa_query_status(sdpa_stream_t stream) {
   cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "stream synchronize");
-  int status = 0, rot_status = 0, qk_status = 0;
+  int status = 0, rot_status = 0, qk_status = 0, bwd_status = 0;
   e = take_prefill_status(&status);
   if (e == cudaSuccess) e = take_rotary_status(&rot_status);
   if (e == cudaSuccess) e = take_qk_status(&qk_status);
+  if (e == cudaSuccess) e = take_bwd_status(&bwd_status);
   if (e != cudaSuccess) return cuda_fail(e, "status read");
   if (!status) status = qk_status;
+  if (!status) status = bwd_status;
   if (status) return fail(SDPA_ERR_TIMEOUT, "a bounded device wait expired (code %d)", status);
   if (rot_status) return fail(SDPA_ERR_INVALID, "a rotary position fell outside its cos/sin cache");
   return SDPA_OK;

@@ -62,6 +62,12 @@ cudaError_t launch_decode(const Problem& p, sdpa_dtype dt, const DecodePlan& pla
                           cudaStream_t st);
 bool decode_supported(sdpa_dtype dt, int H, int Hv);
 
+// Backward (tensor cores): statistics pass, then dK/dV and dQ.  lse2 / delta: B*Nq*S floats.
+bool bwd_tc_supported(const Problem& p, sdpa_dtype dt);
+cudaError_t launch_bwd_tc(const Problem& p, sdpa_dtype dt, const View& dy, const View& dq, const View& dk,
+                          const View& dv, float* lse2, float* delta, cudaStream_t st, const char** name);
+cudaError_t take_bwd_status(int* status);
+
 // Decode with the partials in the library's own device array (no workspace).
 size_t decode_static_scratch_bytes();
 cudaError_t launch_decode_static(const Problem& p, sdpa_dtype dt, const DecodePlan& plan, cudaStream_t st);

@@ -111,8 +111,15 @@ struct TcArgs {
   int add_vec;                                      // bytes per mask load (2, 4, 8 or 16)
   Rules r;
   int q_ds, q_dn, q_db, kv_ds, kv_dn, kv_db;        // tensor-map dimension of seq / head / batch
-  void* y;
+  void* y;                                          // NULL: y is not written (statistics only)
   int64_t y_sb, y_sh, y_ss;
+  // Row statistics for the backward pass (one thread per row only): the log2-sum-exp of the
+  // row in units of q.k scale log2(e), and delta = dY . O (O normalised, fp32), indexed
+  // (b * Nq + h) * S + i.  NULL: not written.
+  float* lse2_out;
+  float* delta_out;
+  const void* dy;
+  int64_t dy_sb, dy_sh, dy_ss;
   const void* q_bias;
   const void* head_sink;
   uint64_t wait_ns;
@@ -834,6 +841,11 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
       const float inv = (denom > 0.f && m_use != -INFINITY) ? 1.f / denom : 0.f;
       T* yrow = reinterpret_cast<T*>(a.y) + (int64_t)b * a.y_sb + (int64_t)qh * a.y_sh + i * a.y_ss +
                 (H / kSplit) * hh;
+      const bool stats = kSplit == 1 && a.lse2_out != nullptr;
+      const T* dyrow = stats ? reinterpret_cast<const T*>(a.dy) + (int64_t)b * a.dy_sb + (int64_t)qh * a.dy_sh +
+                                   i * a.dy_ss
+                             : nullptr;
+      float delta = 0.f;
 #pragma unroll
       for (int c = 0; c < H / (32 * kSplit); ++c) {
         uint32_t o[32];
@@ -844,7 +856,17 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = 0u;
         }
-        if (valid) {
+        if (stats && valid) {
+          // delta = dY . O with O = o / denom in fp32
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 u = *reinterpret_cast<const uint4*>(dyrow + c * 32 + q * 8);
+            const T* e8 = reinterpret_cast<const T*>(&u);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) delta = fmaf(Elem<T>::to_f32(e8[e]), __uint_as_float(o[q * 8 + e]) * inv, delta);
+          }
+        }
+        if (valid && a.y) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint32_t w[4];
@@ -857,6 +879,11 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
             *reinterpret_cast<uint4*>(yrow + c * 32 + q * 8) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
+      }
+      if (stats && valid) {
+        const int64_t r_idx = ((int64_t)b * a.Nq + qh) * a.S + i;
+        a.lse2_out[r_idx] = (denom > 0.f && m_use != -INFINITY) ? m_use + log2f(denom) : INFINITY;
+        a.delta_out[r_idx] = delta;
       }
     }
   }
@@ -996,6 +1023,11 @@ bool tc_eligible(const Problem& p, sdpa_dtype dt) {
 }
 
 cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, const char** name) {
+  return launch_prefill_tc_stats(p, dt, nullptr, nullptr, nullptr, st, name);
+}
+
+cudaError_t launch_prefill_tc_stats(const Problem& p, sdpa_dtype dt, float* lse2, float* delta, const View* dy,
+                                    cudaStream_t st, const char** name) {
   TcArgs a{};
   a.B = p.B; a.Nq = p.Nq; a.Nkv = p.Nkv; a.S = p.S; a.T = (int)p.T; a.group = p.group;
   a.scale = p.scale;
@@ -1031,6 +1063,9 @@ cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, 
   a.r = p.r;
   a.y = const_cast<void*>(p.y.p);
   a.y_sb = p.y.sb; a.y_sh = p.y.sh; a.y_ss = p.y.ss;
+  a.lse2_out = lse2;
+  a.delta_out = delta;
+  if (dy) { a.dy = dy->p; a.dy_sb = dy->sb; a.dy_sh = dy->sh; a.dy_ss = dy->ss; }
   a.q_bias = p.q_bias;
   a.head_sink = p.head_sink;
   a.wait_ns = wait_limit_ns();

@@ -29,6 +29,13 @@ bool tc_make_map(CUtensorMap* map, const View& v, sdpa_dtype dt, int64_t B, int6
 // Launches the fused kernel; p.k / p.v must hold all T key rows (P == 0, no kv bias).
 cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, const char** name);
 
+// The same kernel as the statistics pass of the backward: per query row (index
+// (b * Nq + h) * S + i) the log2-sum-exp of the scores in units of q.k * scale * log2(e)
+// (+inf for a row with nothing admitted) and delta = dY . O, O the normalised output in fp32.
+// y is written only when p.y.p is set.  Interval rules and sink only (no softcap, no masks).
+cudaError_t launch_prefill_tc_stats(const Problem& p, sdpa_dtype dt, float* lse2, float* delta, const View* dy,
+                                    cudaStream_t st, const char** name);
+
 // Reads and clears the device status word the kernel sets when a bounded wait expires.
 cudaError_t take_prefill_status(int* status);
 

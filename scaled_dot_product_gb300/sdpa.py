@@ -34,7 +34,7 @@ SDPA_F32, SDPA_F16, SDPA_BF16 = 0, 1, 2
 SDPA_CAUSAL_NONE, SDPA_CAUSAL_UPPER_LEFT, SDPA_CAUSAL_LOWER_RIGHT = 0, 1, 2
 SDPA_KEEP_NONE, SDPA_KEEP_BOOL_U8, SDPA_KEEP_FILTER_I32 = 0, 1, 2
 SDPA_LEN_NONE, SDPA_LEN_NONPAD_I64, SDPA_LEN_KEYLEN_I32, SDPA_LEN_SEQLENS_K_I32 = 0, 1, 2, 3
-SDPA_OP_FWD, SDPA_OP_DECODE = 0, 1
+SDPA_OP_FWD, SDPA_OP_DECODE, SDPA_OP_BWD = 0, 1, 2
 
 _DTYPES = {torch.float32: SDPA_F32, torch.float16: SDPA_F16, torch.bfloat16: SDPA_BF16}
 CAUSAL = {"none": SDPA_CAUSAL_NONE, "upper_left": SDPA_CAUSAL_UPPER_LEFT,
@@ -84,7 +84,8 @@ class sdpa_params(ctypes.Structure):
 
 EXPORTED = ("sdpa_attn_fwd", "sdpa_attn_decode", "sdpa_workspace_size", "sdpa_validate",
             "sdpa_kv_concat", "sdpa_query_status", "sdpa_last_error", "sdpa_last_kernel_name",
-            "sdpa_version", "sdpa_launch_count", "sdpa_attn_decode_static", "sdpa_rotary")
+            "sdpa_version", "sdpa_launch_count", "sdpa_attn_decode_static", "sdpa_rotary",
+            "sdpa_attn_bwd")
 
 _lib = None
 
@@ -102,6 +103,9 @@ def lib() -> ctypes.CDLL:
         L.sdpa_attn_fwd.restype = ctypes.c_int
         L.sdpa_attn_decode.argtypes = [P, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
         L.sdpa_attn_decode.restype = ctypes.c_int
+        L.sdpa_attn_bwd.argtypes = [P, sdpa_view, sdpa_view, sdpa_view, sdpa_view, ctypes.c_void_p,
+                                    ctypes.c_size_t, ctypes.c_void_p]
+        L.sdpa_attn_bwd.restype = ctypes.c_int
         L.sdpa_attn_decode_static.argtypes = [P, ctypes.c_void_p]
         L.sdpa_attn_decode_static.restype = ctypes.c_int
         L.sdpa_workspace_size.argtypes = [P, ctypes.c_int]
@@ -279,6 +283,25 @@ def sdpa_attn_decode_static(q, k, v, *, y=None, stream=None, **kw) -> torch.Tens
     params, keep = make_params(q, k, v, y=y, **kw)
     _check(lib().sdpa_attn_decode_static(ctypes.byref(params), _stream(stream)))
     return y
+
+
+def sdpa_attn_bwd(q, k, v, dy, *, dq=None, dk=None, dv=None, workspace=None, stream=None, **kw):
+    """Backward over 4-D (B, N, S, D) CUDA views: returns (dq, dk, dv) for the upstream
+    gradient dy (B, Nq, S, Hv).  Keyword arguments describe the forward problem as for
+    sdpa_attn_fwd (head_sink, scale, causal, window, lens / len_kind)."""
+    B, Nq, S, H = q.shape
+    Nkv, L, Hv = k.shape[1], k.shape[2], v.shape[3]
+    if dq is None:
+        dq = torch.empty(B, Nq, S, H, dtype=q.dtype, device=q.device)
+    if dk is None:
+        dk = torch.empty(B, Nkv, L, H, dtype=q.dtype, device=q.device)
+    if dv is None:
+        dv = torch.empty(B, Nkv, L, Hv, dtype=q.dtype, device=q.device)
+    params, keep = make_params(q, k, v, **kw)
+    ws, nbytes = _workspace(params, SDPA_OP_BWD, workspace, q.device)
+    _check(lib().sdpa_attn_bwd(ctypes.byref(params), _view(dy, keep), _view(dq, keep), _view(dk, keep),
+                               _view(dv, keep), None if ws is None else ws.data_ptr(), nbytes, _stream(stream)))
+    return dq, dk, dv
 
 
 def sdpa_kv_concat(past: Optional[torch.Tensor], cur: torch.Tensor, present: torch.Tensor,

@@ -219,6 +219,13 @@ def make_case(name: str, *, dtype=torch.bfloat16, B=1, Nq=2, Nkv=None, S=16, L=N
                 rotary_interleaved=rotary == "interleaved", seed=seed)
 
 
+def draw_dy(case: Case, seed: int) -> torch.Tensor:
+    """Upstream gradient dY for the backward, in y's layout (rank-3 when the query is
+    packed): N(0, 1) drawn in fp32 from its own seeded generator, rounded once to the dtype."""
+    gen = torch.Generator().manual_seed(seed)
+    return _normal(gen, case.y_shape(), case.dtype)
+
+
 @dataclass
 class RotaryInputs:
     """Inputs of one standalone RotaryEmbedding call."""

@@ -271,3 +271,50 @@ def test_qk_output_validation():
     over = q.view(torch.float32)[..., :8]                    # inside q's bytes
     p, keep = sdpa.make_params(q, k, v, y=y, qk_out=over)
     assert sdpa.sdpa_validate(p) == sdpa.SDPA_ERR_ALIAS
+
+
+# ----------------------------------------------------------------- backward (host checks only)
+
+def test_backward_subset_validates():
+    assert code(base(), sdpa.SDPA_OP_BWD) == sdpa.SDPA_OK
+    assert code(base(H=128, Hv=128, causal="lower_right", window=4), sdpa.SDPA_OP_BWD) == sdpa.SDPA_OK
+    assert code(base(causal="upper_left", lens=torch.tensor([3, 8]), len_kind="nonpad"), sdpa.SDPA_OP_BWD) == sdpa.SDPA_OK
+    assert code(base(dtype=torch.float16, head_sink=torch.zeros(4, dtype=torch.float16)), sdpa.SDPA_OP_BWD) == sdpa.SDPA_OK
+
+
+@pytest.mark.parametrize("kw,why", [
+    (dict(softcap=30.0), "softcap"),
+    (dict(dtype=torch.float32, H=64, Hv=64), "f32"),
+    (dict(H=96, Hv=96), "head size"),
+    (dict(H=64, Hv=128), "H != Hv"),
+    (dict(P=5), "past rows"),
+    (dict(keep_mask=torch.ones(1, 1, 8, 8, dtype=torch.uint8), keep_kind="bool"), "bool mask"),
+    (dict(add_mask=torch.zeros(1, 1, 8, 8, dtype=torch.bfloat16)), "float mask"),
+    (dict(lens=torch.tensor([3, 8], dtype=torch.int32), len_kind="keylen"), "key-padding lengths"),
+])
+def test_backward_rejects_outside_its_subset(kw, why):
+    assert code(base(**kw), sdpa.SDPA_OP_BWD) == sdpa.SDPA_ERR_UNSUPPORTED, why
+
+
+def test_backward_rejects_present_outputs():
+    pk = torch.zeros(2, 2, 8, 64, dtype=torch.bfloat16)
+    pv = torch.zeros(2, 2, 8, 64, dtype=torch.bfloat16)
+    assert code(base(present_k=pk, present_v=pv), sdpa.SDPA_OP_BWD) == sdpa.SDPA_ERR_INVALID
+
+
+def test_backward_workspace_is_two_floats_per_query_row():
+    params, _keep = base(B=3, Nq=4, S=100)
+    assert sdpa.sdpa_workspace_size(params, sdpa.SDPA_OP_BWD) == 2 * ((3 * 4 * 100 * 4 + 255) // 256 * 256)
+    params, _keep = base(softcap=5.0)
+    assert sdpa.sdpa_workspace_size(params, sdpa.SDPA_OP_BWD) == 0
+
+
+def test_backward_gradient_alias_is_rejected_before_launch():
+    """dq overlapping q is refused on the host (no device work is enqueued)."""
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    k = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    v = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    dy = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(sdpa.SdpaError) as e:
+        sdpa.sdpa_attn_bwd(q, k, v, dy, dq=q, workspace=torch.zeros(4096, dtype=torch.uint8), stream=0)
+    assert e.value.code == sdpa.SDPA_ERR_ALIAS
