@@ -11,6 +11,8 @@
 // query row, the log2-sum-exp L_i of its scores and delta_i = dY_i . O_i (= rowsum(P dP)).
 // Then two kernels recompute the scores tile by tile, so no S x T matrix is stored:
 //
+// The score scale of dS is applied once, to the accumulated dQ and dK when they are stored.
+//
 //   bwd_dkdv_kernel   one CTA per (128-key tile, kv head, batch); loops over the query
 //                     tiles and the grouped query heads that see the key tile:
 //                       S^T = K Q^T, dP^T = V dY^T            (tcgen05, both operands in smem)
@@ -143,14 +145,17 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // One 128 x 128 tile of scores and score gradients in TMEM (this thread's lane = one row):
-// P = 2^(s scale log2e - L) on admitted entries, dS = P (dP - delta) scale; P goes over the
-// first 64 columns of S and dS over the first 64 columns of dP, as packed 16-bit pairs.
-// Entry e of the row is admitted when e_lo <= e <= e_hi; L and delta come per entry from
-// shared memory (per_col) or are the row's own (!per_col).
-template <bool kBF16, bool kWantP>
-__device__ __forceinline__ void grad_tile(uint32_t tS, uint32_t tdP, float scale, float scale_log2, int e_lo,
-                                          int e_hi, bool per_col, float L_row, float d_row, const float* L_col,
-                                          const float* d_col) {
+// P = 2^(s scale log2e - L) on admitted entries and dS' = P (dP - delta) (the score scale is
+// applied once to the accumulated dQ / dK instead); P goes over the first 64 columns of S and
+// dS' over the first 64 columns of dP (or of S when P is not wanted), as packed 16-bit pairs.
+// Entry e of the row is admitted when e_lo <= e <= e_hi (full: every entry); -L and -delta
+// come per entry from shared memory (kPerCol) or are the row's own.
+template <bool kBF16, bool kWantP, bool kPerCol>
+__device__ __forceinline__ void grad_tile(uint32_t tS, uint32_t tdP, float scale_log2, int e_lo, int e_hi,
+                                          bool full, float nL_row, float nd_row, const float* nL_col,
+                                          const float* nd_col) {
+  const f2_t sl2 = f2_pack(scale_log2, scale_log2);
+  const f2_t nL_r = f2_pack(nL_row, nL_row), nd_r = f2_pack(nd_row, nd_row);
 #pragma unroll 1
   for (int c = 0; c < 4; ++c) {
     uint32_t us[32], ud[32];
@@ -160,19 +165,28 @@ __device__ __forceinline__ void grad_tile(uint32_t tS, uint32_t tdP, float scale
     uint32_t pw[16], dw[16];
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
-      float p2[2], g2[2];
-#pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int col = c * 32 + e + h;
-        const float L = per_col ? L_col[col] : L_row;
-        const float d = per_col ? d_col[col] : d_row;
-        float p = ex2_approx(fmaf(__uint_as_float(us[e + h]), scale_log2, -L));
-        if (col < e_lo || col > e_hi) p = 0.f;
-        p2[h] = p;
-        g2[h] = p * (__uint_as_float(ud[e + h]) - d) * scale;
+      const int col = c * 32 + e;
+      f2_t nL = nL_r, nd = nd_r;
+      if constexpr (kPerCol) {
+        const float2 Lv = *reinterpret_cast<const float2*>(nL_col + col);
+        const float2 dv = *reinterpret_cast<const float2*>(nd_col + col);
+        nL = f2_pack(Lv.x, Lv.y);
+        nd = f2_pack(dv.x, dv.y);
       }
-      if constexpr (kWantP) pw[e >> 1] = pack2<kBF16>(p2[0], p2[1]);
-      dw[e >> 1] = pack2<kBF16>(g2[0], g2[1]);
+      float p0, p1;
+      f2_unpack(f2_fma(f2_pack(__uint_as_float(us[e]), __uint_as_float(us[e + 1])), sl2, nL), p0, p1);
+      p0 = ex2_approx(p0);
+      p1 = ex2_approx(p1);
+      if (!full) {
+        if (col < e_lo || col > e_hi) p0 = 0.f;
+        if (col + 1 < e_lo || col + 1 > e_hi) p1 = 0.f;
+      }
+      const f2_t pp = f2_pack(p0, p1);
+      const f2_t g = f2_mul(pp, f2_add(f2_pack(__uint_as_float(ud[e]), __uint_as_float(ud[e + 1])), nd));
+      float g0, g1;
+      f2_unpack(g, g0, g1);
+      if constexpr (kWantP) pw[e >> 1] = pack2<kBF16>(p0, p1);
+      dw[e >> 1] = pack2<kBF16>(g0, g1);
     }
     // chunk c's 16 packed columns land in columns already read (16c..16c+15 < 32(c+1))
     if constexpr (kWantP) tmem_st16(tS + c * 16, pw);
@@ -181,9 +195,10 @@ __device__ __forceinline__ void grad_tile(uint32_t tS, uint32_t tdP, float scale
   tmem_st_wait();
 }
 
-// Writes a 128-lane accumulator row (D columns, fp32 in TMEM) as 16-bit values, or zeros.
+// Writes a 128-lane accumulator row (D columns, fp32 in TMEM) times mul as 16-bit values,
+// or zeros.
 template <int D, bool kBF16>
-__device__ __forceinline__ void store_row(uint32_t tAcc, bool have, bool valid, void* dst) {
+__device__ __forceinline__ void store_row(uint32_t tAcc, bool have, bool valid, float mul, void* dst) {
   using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
   T* out = reinterpret_cast<T*>(dst);
 #pragma unroll
@@ -202,7 +217,7 @@ __device__ __forceinline__ void store_row(uint32_t tAcc, bool have, bool valid, 
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-          w[e] = pack2<kBF16>(__uint_as_float(o[q * 8 + 2 * e]), __uint_as_float(o[q * 8 + 2 * e + 1]));
+          w[e] = pack2<kBF16>(__uint_as_float(o[q * 8 + 2 * e]) * mul, __uint_as_float(o[q * 8 + 2 * e + 1]) * mul);
         *reinterpret_cast<uint4*>(out + c * 32 + q * 8) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
@@ -223,7 +238,7 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
   __shared__ __align__(8) uint64_t bar_full[C::kStages], bar_empty[C::kStages];
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_flag;
-  __shared__ float sh_L[2][kBM], sh_d[2][kBM];
+  __shared__ __align__(16) float sh_L[2][kBM], sh_d[2][kBM];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   // work unit: key tile (heavy first under causal rules), then (batch, kv head)
@@ -380,8 +395,8 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
           L = a.lse2[idx];
           d = a.delta[idx];
         }
-        sh_L[n & 1][row] = L;
-        sh_d[n & 1][row] = d;
+        sh_L[n & 1][row] = -L;
+        sh_d[n & 1][row] = -d;
         const uint32_t bst = smem_u32(&bar_stat[n & 1]);
         mbar_arrive(bst);
         if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(bst, (n >> 1) & 1, abortp, a.wait_ns)))) break;
@@ -390,7 +405,8 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
       tc_fence_after();
       const int e_lo = (int)bmax(-1, bmin((int64_t)kBM, qlo - q0));
       const int e_hi = (int)bmax(-1, bmin((int64_t)kBM, qhi - q0));
-      grad_tile<kBF16, true>(tS, tP, a.scale, a.scale_log2, e_lo, e_hi, true, 0.f, 0.f, sh_L[n & 1], sh_d[n & 1]);
+      const bool full = __all_sync(0xffffffffu, e_lo <= 0 && e_hi >= kBM - 1);
+      grad_tile<kBF16, true, true>(tS, tP, a.scale_log2, e_lo, e_hi, full, 0.f, 0.f, sh_L[n & 1], sh_d[n & 1]);
       tc_fence_before();
       mbar_arrive(b_pready);
     }
@@ -400,8 +416,8 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
       const bool valid = j < a.T;
       char* dk = reinterpret_cast<char*>(a.out0) + (b * a.o0_sb + (int64_t)kvh * a.o0_sh + j * a.o0_ss) * 2;
       char* dv = reinterpret_cast<char*>(a.out1) + (b * a.o1_sb + (int64_t)kvh * a.o1_sh + j * a.o1_ss) * 2;
-      store_row<H, kBF16>(trow + C::kTmemA0, n_steps > 0, valid, dk);
-      store_row<H, kBF16>(trow + C::kTmemA1, n_steps > 0, valid, dv);
+      store_row<H, kBF16>(trow + C::kTmemA0, n_steps > 0, valid, a.scale, dk);
+      store_row<H, kBF16>(trow + C::kTmemA1, n_steps > 0, valid, 1.f, dv);
     }
   }
 
@@ -565,7 +581,8 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
       const int64_t key0 = (int64_t)(kt0 + n) * kBM;
       const int e_lo = (int)bmax(-1, bmin((int64_t)kBM, lo - key0));
       const int e_hi = (int)bmax(-1, bmin((int64_t)kBM, hi - key0));
-      grad_tile<kBF16, false>(tS, tP, a.scale, a.scale_log2, e_lo, e_hi, false, L, d, nullptr, nullptr);
+      const bool full = __all_sync(0xffffffffu, e_lo <= 0 && e_hi >= kBM - 1);
+      grad_tile<kBF16, false, false>(tS, tP, a.scale_log2, e_lo, e_hi, full, -L, -d, nullptr, nullptr);
       tc_fence_before();
       mbar_arrive(b_pready);
     }
@@ -573,7 +590,7 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
     if (ok) {
       tc_fence_after();
       char* dq = reinterpret_cast<char*>(a.out0) + (b * a.o0_sb + (int64_t)qh * a.o0_sh + i * a.o0_ss) * 2;
-      store_row<H, kBF16>(trow + C::kTmemA0, n_steps > 0, valid, dq);
+      store_row<H, kBF16>(trow + C::kTmemA0, n_steps > 0, valid, a.scale, dq);
     }
   }
 

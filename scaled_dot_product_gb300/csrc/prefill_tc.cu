@@ -258,7 +258,7 @@ __device__ __noinline__ float generic_score(const Rules& r, const RowCtx& ctx, f
 // then at least 2^(-2 c log2 e), a normal number in fp32 and bf16 for c <= 40.
 enum RuleMode { kPlain = 0, kAddMask = 1, kGeneric = 2, kCapFixed = 3 };
 
-template <int H, bool kBF16, int kMode, int QT, int SPLIT>
+template <int H, bool kBF16, int kMode, int QT, int SPLIT, bool kStats>
 __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>::kMinBlocks)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const TcArgs a) {
@@ -841,7 +841,7 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
       const float inv = (denom > 0.f && m_use != -INFINITY) ? 1.f / denom : 0.f;
       T* yrow = reinterpret_cast<T*>(a.y) + (int64_t)b * a.y_sb + (int64_t)qh * a.y_sh + i * a.y_ss +
                 (H / kSplit) * hh;
-      const bool stats = kSplit == 1 && a.lse2_out != nullptr;
+      constexpr bool stats = kStats && kSplit == 1;   // the backward's statistics pass
       const T* dyrow = stats ? reinterpret_cast<const T*>(a.dy) + (int64_t)b * a.dy_sb + (int64_t)qh * a.dy_sh +
                                    i * a.dy_ss
                              : nullptr;
@@ -866,7 +866,7 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
             for (int e = 0; e < 8; ++e) delta = fmaf(Elem<T>::to_f32(e8[e]), __uint_as_float(o[q * 8 + e]) * inv, delta);
           }
         }
-        if (valid && a.y) {
+        if (valid && (!kStats || a.y)) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint32_t w[4];
@@ -954,7 +954,7 @@ uint64_t wait_limit_ns() {
   return v;
 }
 
-template <int H, bool kBF16, int kMode, int QT, int SPLIT>
+template <int H, bool kBF16, int kMode, int QT, int SPLIT, bool kStats = false>
 cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, TcArgs a,
                         int64_t units_per_qt_row, cudaStream_t st) {
   using C = Cfg<H, QT>;
@@ -962,19 +962,19 @@ cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, kBF16, kMode, QT, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, kBF16, kMode, QT, SPLIT, kStats>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     C::kSmem);
     // the in-kernel register split assumes the block is launched with kLaunchRegs per
     // thread; with fewer, the softmax warps' request could never be met
     cudaFuncAttributes fa{};
-    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<H, kBF16, kMode, QT, SPLIT>);
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<H, kBF16, kMode, QT, SPLIT, kStats>);
     if (attr_err == cudaSuccess && fa.numRegs < Lay::kLaunchRegs) attr_err = cudaErrorLaunchOutOfResources;
   });
   if (attr_err != cudaSuccess) return attr_err;
   a.nunits = (a.S + QT * kBM - 1) / (QT * kBM);
   const int64_t units = units_per_qt_row * a.nunits;
   if (units > 0x7fffffff) return cudaErrorInvalidValue;
-  prefill_tc_kernel<H, kBF16, kMode, QT, SPLIT><<<(unsigned)units, Lay::kThreads, C::kSmem, st>>>(tq, tk, tv, a);
+  prefill_tc_kernel<H, kBF16, kMode, QT, SPLIT, kStats><<<(unsigned)units, Lay::kThreads, C::kSmem, st>>>(tq, tk, tv, a);
   count_launch(1);
   return cudaGetLastError();
 }
@@ -984,6 +984,11 @@ cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
 template <int H, bool kBF16>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TcArgs& a,
                      int64_t heads_batches, cudaStream_t st) {
+  if (a.lse2_out) {
+    // the backward's statistics pass: interval rules only (the backward rejects the rest)
+    if (a.generic || a.add_fast || a.has_softcap) return cudaErrorInvalidValue;
+    return launch_mode<H, kBF16, kPlain, 1, 1, true>(tq, tk, tv, a, heads_batches, st);
+  }
   if (a.generic) return launch_mode<H, kBF16, kGeneric, 2, 1>(tq, tk, tv, a, heads_batches, st);
   if (a.add_fast) return launch_mode<H, kBF16, kAddMask, 2, 1>(tq, tk, tv, a, heads_batches, st);
   if constexpr (kBF16)
