@@ -156,6 +156,7 @@ KERNEL_SOURCES = {
     "decode_splitkv": ("decode.cu", "internal.h", "common.cuh"),
     "rotary": ("rotary.cu", "internal.h", "common.cuh"),
     "qk_tc": ("qk.cu", "prefill_tc.h", "tc_ptx.cuh", "common.cuh"),
+    "bwd_tc": ("bwd_tc.cu", "prefill_tc.cu", "prefill_tc.h", "tc_ptx.cuh", "common.cuh", "internal.h"),
 }
 
 

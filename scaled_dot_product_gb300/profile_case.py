@@ -3,6 +3,7 @@
     python -m scaled_dot_product_gb300.profile_case --workload 2 [--batch B] [--rope]
         [--qk-mode M] [--iters K]
     python -m scaled_dot_product_gb300.profile_case --rotary [--iters K]
+    python -m scaled_dot_product_gb300.profile_case --workload 3 --backward [--iters K]
 
 Inputs are the seeded synthetic workloads of scaled_dot_product_gb300.workloads; every
 launch goes through the C ABI (libsdpa.so).  Prints the kernel names and the status word.
@@ -14,7 +15,7 @@ import argparse
 import torch
 
 from . import sdpa
-from .workloads import WORKLOADS, make_rotary_inputs, rope_caches, workload
+from .workloads import WORKLOADS, as4d, draw_dy, make_rotary_inputs, rope_caches, workload
 
 
 def main():
@@ -24,6 +25,7 @@ def main():
     ap.add_argument("--rope", action="store_true", help="rotate Q and the new K rows first")
     ap.add_argument("--qk-mode", type=int, default=None, help="also write the qk output at this stage")
     ap.add_argument("--rotary", action="store_true", help="standalone rotary (bf16, B=4, S=4096, 32 x 128)")
+    ap.add_argument("--backward", action="store_true", help="the backward (sdpa_attn_bwd) of the workload")
     ap.add_argument("--iters", type=int, default=3)
     a = ap.parse_args()
     torch.cuda.set_device(0)
@@ -33,6 +35,13 @@ def main():
         y = torch.empty_like(ri.x)
         for _ in range(a.iters):
             sdpa.sdpa_rotary(ri.x, ri.cos, ri.sin, ri.position_ids, num_heads=32, y=y)
+    elif a.backward:
+        case_cpu = workload(a.workload, batch=a.batch)
+        case = case_cpu.to("cuda")
+        q, k, v = case.views()
+        dy = as4d(draw_dy(case_cpu, seed=3000 + a.workload).to("cuda"), case.q_layout, case.Nq)
+        for _ in range(a.iters):
+            sdpa.sdpa_attn_bwd(q, k, v, dy, **sdpa.case_kwargs(case))
     else:
         case = workload(a.workload, batch=a.batch)
         if a.rope:
