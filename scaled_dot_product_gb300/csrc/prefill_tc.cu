@@ -109,6 +109,9 @@ struct TcArgs {
   int generic;                                      // per-element rules beyond the structural ones
   int add_fast;                                     // additive mask only: vectorised path
   int add_vec;                                      // bytes per mask load (2, 4, 8 or 16)
+  int keep_fast;                                    // keep mask / key-length filter, no float mask
+  int keep_vec;                                     // keep-mask rows allow 16-byte loads
+  float filter_raw;                                 // mask_filter_value in units of raw q.k
   Rules r;
   int q_ds, q_dn, q_db, kv_ds, kv_dn, kv_db;        // tensor-map dimension of seq / head / batch
   void* y;                                          // NULL: y is not written (statistics only)
@@ -256,7 +259,63 @@ __device__ __noinline__ float generic_score(const Rules& r, const RowCtx& ctx, f
 // capped logits lie in [-c, c], so the softmax uses the fixed maximum c (log2 domain: c log2 e)
 // instead of a running one: no row maximum, no rescale of the accumulator.  Every weight is
 // then at least 2^(-2 c log2 e), a normal number in fp32 and bf16 for c <= 40.
-enum RuleMode { kPlain = 0, kAddMask = 1, kGeneric = 2, kCapFixed = 3 };
+// kKeep: interval rules plus a keep mask (ai.onnx BOOL attn_mask, MultiHeadAttention binary
+// key mask) and MultiHeadAttention key-padding lengths, neither softcap nor a float mask.
+enum RuleMode { kPlain = 0, kAddMask = 1, kGeneric = 2, kCapFixed = 3, kKeep = 4 };
+
+// Keep bits of keys [k0, k0 + 128) of one keep-mask row (bit e of word e / 32 set = keep);
+// keys >= T_keep count as not kept.  u8 rows (bool) or int32 rows (binary), any non-zero
+// value keeps.
+__device__ __forceinline__ void keep_bits128(const void* row, bool is_u8, int k0, int64_t T_keep, bool vec,
+                                             uint32_t* kb) {
+  if (vec && (int64_t)k0 + 128 <= T_keep) {
+    if (is_u8) {
+      const uint4* p = reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(row) + k0);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint4 lo = __ldg(p + 2 * w), hi = __ldg(p + 2 * w + 1);
+        const uint32_t words[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+        uint32_t bits = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint32_t m = __vcmpne4(words[q], 0u);   // 0xff per non-zero byte
+          const uint32_t nib = ((m >> 7) & 1u) | ((m >> 14) & 2u) | ((m >> 21) & 4u) | ((m >> 28) & 8u);
+          bits |= nib << (4 * q);
+        }
+        kb[w] = bits;
+      }
+    } else {
+      const uint4* p = reinterpret_cast<const uint4*>(reinterpret_cast<const int32_t*>(row) + k0);
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        uint32_t bits = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const uint4 u = __ldg(p + 8 * w + q);
+          bits |= ((u.x != 0u) ? 1u : 0u) << (4 * q);
+          bits |= ((u.y != 0u) ? 2u : 0u) << (4 * q);
+          bits |= ((u.z != 0u) ? 4u : 0u) << (4 * q);
+          bits |= ((u.w != 0u) ? 8u : 0u) << (4 * q);
+        }
+        kb[w] = bits;
+      }
+    }
+  } else {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      uint32_t bits = 0;
+      for (int q = 0; q < 32; ++q) {
+        const int64_t key = (int64_t)k0 + 32 * w + q;
+        bool keep = false;
+        if (key < T_keep)
+          keep = is_u8 ? (reinterpret_cast<const uint8_t*>(row)[key] != 0)
+                       : (reinterpret_cast<const int32_t*>(row)[key] != 0);
+        bits |= (keep ? 1u : 0u) << q;
+      }
+      kb[w] = bits;
+    }
+  }
+}
 
 template <int H, bool kBF16, int kMode, int QT, int SPLIT, bool kStats>
 __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>::kMinBlocks)
@@ -515,6 +574,11 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
     ctx.len = len_b;
     ctx.pos = pos_of(a, len_b, i);
     const void* mrow = nullptr;
+    if (kMode == kKeep && valid && a.r.keep_kind != SDPA_KEEP_NONE) {
+      const int esz = a.r.keep_kind == SDPA_KEEP_BOOL_U8 ? 1 : 4;
+      mrow = reinterpret_cast<const char*>(a.r.keep) +
+             (b * a.r.keep_sb + (int64_t)qh * a.r.keep_sh + i * a.r.keep_ss) * esz;
+    }
     if (kMode == kAddMask && valid) {
       const int esz = a.r.add_dtype == SDPA_F32 ? 4 : 2;
       mrow = reinterpret_cast<const char*>(a.r.add) +
@@ -528,7 +592,8 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
     // scale or the softcap amplitude, additive-mask scores are in natural units, and the
     // generic mode produces log2-domain scores already
     const float kfac = (kMode == kPlain) ? (a.has_softcap ? a.cap_out_log2 : a.scale_log2)
-                                         : (kMode == kAddMask ? kLog2e : 1.f);
+                       : (kMode == kKeep) ? a.scale_log2
+                                          : (kMode == kAddMask ? kLog2e : 1.f);
     // kCapFixed: the fixed maximum (the cap, or the sink logit when that is larger)
     float m_fixed = a.cap_out_log2;
     if (kMode == kCapFixed && a.head_sink)
@@ -572,6 +637,11 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
         // fetch this row's mask values for the tile now; the wait below hides the latency
         if (valid)
           prefetch_mask128(reinterpret_cast<const T*>(mrow), (kv_t0 + j) * kBN, a.r.add_T, a.add_vec, mraw);
+      }
+      uint32_t kb[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};   // keep bits
+      if constexpr (kMode == kKeep) {
+        if (mrow)
+          keep_bits128(mrow, a.r.keep_kind == SDPA_KEEP_BOOL_U8, (kv_t0 + j) * kBN, a.r.keep_T, a.keep_vec != 0, kb);
       }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_sfull(x), j & 1, abortp, a.wait_ns)))) break;
       tc_fence_after();
@@ -682,6 +752,24 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
           const int elo = lo32 - key0, ehi = hi32 - key0;
 #pragma unroll
           for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
+        }
+      } else if constexpr (kMode == kKeep) {
+        // raw scores: a key the keep mask drops is excluded (bool) or gets the filter value
+        // (binary), as does every key at or past a key-padding length; then the bounds
+        const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
+        const bool all_keep = (kb[0] & kb[1] & kb[2] & kb[3]) == 0xffffffffu;
+        const int len_e = (a.r.len_kind == SDPA_LEN_KEYLEN_I32) ? (int)max64(-1, min64(len_b - key0, kHalf)) : kHalf;
+        if (!__all_sync(0xffffffffu, full && all_keep && len_e >= kHalf)) {
+          const bool drop_excludes = a.r.keep_kind == SDPA_KEEP_BOOL_U8;
+          const float fr = a.filter_raw;
+          const int elo = lo32 - key0, ehi = hi32 - key0;
+#pragma unroll
+          for (int e = 0; e < kHalf; ++e) {
+            float v = s[e];
+            if (!((kb[e >> 5] >> (e & 31)) & 1u)) v = drop_excludes ? -INFINITY : v + fr;
+            if (e >= len_e) v += fr;
+            s[e] = (e >= elo && e <= ehi) ? v : -INFINITY;
+          }
         }
       } else if constexpr (kMode == kAddMask) {
         // additive mask / attention bias, then softcap (or the reverse), then the bounds;
@@ -990,6 +1078,7 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     return launch_mode<H, kBF16, kPlain, 1, 1, true>(tq, tk, tv, a, heads_batches, st);
   }
   if (a.generic) return launch_mode<H, kBF16, kGeneric, 2, 1>(tq, tk, tv, a, heads_batches, st);
+  if (a.keep_fast) return launch_mode<H, kBF16, kKeep, 1, 1>(tq, tk, tv, a, heads_batches, st);
   if (a.add_fast) return launch_mode<H, kBF16, kAddMask, 2, 1>(tq, tk, tv, a, heads_batches, st);
   if constexpr (kBF16)
     if (a.cap_fixed) return launch_mode<H, kBF16, kCapFixed, 1, 1>(tq, tk, tv, a, heads_batches, st);
@@ -1052,7 +1141,18 @@ cudaError_t launch_prefill_tc_stats(const Problem& p, sdpa_dtype dt, float* lse2
   a.len_kind = p.r.len_kind;
   a.lens = p.r.lens;
   const bool other_rules = (p.r.keep_kind != SDPA_KEEP_NONE) || (p.r.len_kind == SDPA_LEN_KEYLEN_I32);
-  a.generic = other_rules;
+  a.keep_fast = other_rules && p.r.add == nullptr && !a.has_softcap;
+  a.generic = other_rules && !a.keep_fast;
+  if (a.keep_fast) {
+    a.filter_raw = p.r.filter / p.scale;
+    if (p.r.keep_kind != SDPA_KEEP_NONE) {
+      // 16-byte loads need every row start 16-byte aligned (key offsets are multiples of 128)
+      const int64_t esz = p.r.keep_kind == SDPA_KEEP_BOOL_U8 ? 1 : 4;
+      uint64_t g = reinterpret_cast<uintptr_t>(p.r.keep);
+      for (int64_t st : {p.r.keep_sb, p.r.keep_sh, p.r.keep_ss}) g |= (uint64_t)(st * esz);
+      a.keep_vec = (g & 15u) == 0;
+    }
+  }
   a.add_fast = (p.r.add != nullptr) && !other_rules && p.r.add_dtype == (int)dt;
   if (p.r.add != nullptr && !a.add_fast) a.generic = 1;
   if (a.add_fast) {
@@ -1064,7 +1164,7 @@ cudaError_t launch_prefill_tc_stats(const Problem& p, sdpa_dtype dt, float* lse2
     a.add_vec = (int)(g & (~g + 1));   // lowest set bit
     if (a.add_vec > 16) a.add_vec = 16;
   }
-  a.cap_fixed = dt == SDPA_BF16 && a.has_softcap && p.r.softcap <= 40.f && !a.generic && !a.add_fast;
+  a.cap_fixed = dt == SDPA_BF16 && a.has_softcap && p.r.softcap <= 40.f && !a.generic && !a.add_fast && !a.keep_fast;
   a.r = p.r;
   a.y = const_cast<void*>(p.y.p);
   a.y_sb = p.y.sb; a.y_sh = p.y.sh; a.y_ss = p.y.ss;

@@ -275,6 +275,9 @@ WORKLOADS = {
     3: "gqa_bf16_b1_s4096_q64_kv8_h64_window1024_sink",
     4: "mha_decode_f16_b64_n32_h128_past4095_keylen",
     5: "mha_cross_f16_b8_s448_n20_h64_kv1500_bias",
+    # not a headline configuration: measures MultiHeadAttention's binary key mask and
+    # unidirectional (lower-right causal) rule on the tensor-core path
+    6: "mha_prefill_f16_b4_s2048_n16_h128_binary_mask_unidirectional",
 }
 
 
@@ -310,6 +313,12 @@ def workload(idx: int, small: bool = False, seed: Optional[int] = None, batch: O
         return make_case(name, dtype=torch.float16, B=B, Nq=N, S=S, L=Lk, H=H,
                          q_layout="bsnh", kv_layout="bnsh", seed=seed, qkv_bias="q",
                          add_mask="float", add_mask_shape=(B, 1, S, Lk), add_mask_range=(-1.0, 0.0))
+    if idx == 6:
+        B, S, N, H = (2, 300, 4, 128) if small else (4, 2048, 16, 128)
+        B = batch if batch is not None else B
+        return make_case(name, dtype=torch.float16, B=B, Nq=N, S=S, H=H, q_layout="bsnh", kv_layout="bsnh",
+                         seed=seed, causal="lower_right", keep_kind="filter", keep_mask_shape=(B, 1, S, S),
+                         keep_density=0.9)
     raise KeyError(idx)
 
 

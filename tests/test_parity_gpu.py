@@ -61,7 +61,7 @@ def run_and_compare(case: Case, op: str = "fwd", rows=None):
 
 # ----------------------------------------------------------------- the five workloads, small
 
-@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5])
+@pytest.mark.parametrize("idx", [1, 2, 3, 4, 5, 6])
 def test_workload_small_fwd(idx):
     run_and_compare(workload(idx, small=True), "fwd")
 
@@ -214,7 +214,7 @@ def _sample_rows(case: Case, n: int, seed: int) -> np.ndarray:
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("idx,op", [(2, "fwd"), (3, "fwd"), (4, "decode"), (4, "fwd"), (5, "fwd")])
+@pytest.mark.parametrize("idx,op", [(2, "fwd"), (3, "fwd"), (4, "decode"), (4, "fwd"), (5, "fwd"), (6, "fwd")])
 def test_workload_full_size_sampled(idx, op):
     case = workload(idx)
     run_and_compare(case, op, rows=_sample_rows(case, 96, 100 + idx))
@@ -243,3 +243,34 @@ def test_bf16_softcap_fixed_maximum(H, softcap, q_gain, sink):
         c.head_sink = (torch.arange(c.Nq, dtype=torch.float32) * 3.0 + softcap + 2.0).to(torch.bfloat16)
     err, name = run_and_compare(c, "fwd")
     assert name.startswith("prefill_tc"), name
+
+
+# ----------------------------------------------------------------- keep masks on the tensor-core path
+
+@pytest.mark.parametrize("kw", [
+    dict(name="bool_ul_bf16_h128", dtype=torch.bfloat16, H=128, causal="upper_left", keep_kind="bool",
+         keep_mask_shape=(2, 1, 200, 320)),
+    dict(name="bool_short_f16_h64", dtype=torch.float16, H=64, keep_kind="bool",
+         keep_mask_shape=(1, 4, 200, 301)),                 # rows not 16-byte aligned, shorter than T
+    dict(name="filter_lr_f16_h128", dtype=torch.float16, H=128, causal="lower_right", keep_kind="filter",
+         keep_mask_shape=(2, 1, 200, 320)),
+    dict(name="filter_keylen_bf16_h64", dtype=torch.bfloat16, H=64, keep_kind="filter",
+         keep_mask_shape=(2, 1, 1, 320), len_kind="keylen", len_range=(5, 320)),
+    dict(name="keylen_only_f16_h128", dtype=torch.float16, H=128, causal="lower_right", len_kind="keylen",
+         len_range=(1, 320), sink=True),
+    dict(name="bool_window_gqa_bf16_h64", dtype=torch.bfloat16, H=64, Nkv=2, causal="lower_right", window=90,
+         keep_kind="bool", keep_mask_shape=(2, 4, 200, 320)),
+])
+def test_keep_masks_tensor_core_path(kw):
+    kw = dict(kw)
+    name = kw.pop("name")
+    kw.setdefault("Nkv", 4)
+    case = make_case(name, B=2, Nq=4, S=200, L=320, seed=60 + len(name), keep_density=0.85, **kw)
+    err, kernel = run_and_compare(case, "fwd")
+    assert kernel.startswith("prefill_tc"), kernel
+
+
+def test_keep_mask_excluding_whole_rows_gives_zeros():
+    c = make_case("bool_allfalse", dtype=torch.bfloat16, B=1, Nq=2, S=150, L=150, H=64, seed=71,
+                  keep_kind="bool", keep_mask_shape=(1, 1, 150, 150), keep_density=0.0)
+    run_and_compare(c, "fwd")
