@@ -64,17 +64,23 @@ struct BwdArgs {
   uint64_t wait_ns;
 };
 
-template <int H>
+// H: head size; STEP: rows of the streamed tiles (the queries of one dK/dV step, the keys of
+// one dQ step).  With STEP = 64 and H = 64 a CTA needs 256 TMEM columns and 96 KB of shared
+// memory, so two CTAs share an SM and one's score pass runs under the other's products.
+template <int H, int STEP>
 struct BCfg {
-  static constexpr int kRegions = H / 64;          // 128-byte swizzle regions per row
-  static constexpr int kRegionBytes = 128 * 128;   // 128 rows x 128 bytes
-  static constexpr int kTile = kBM * H * 2;        // one 128-row tile of 16-bit elements
+  static constexpr int kRegions = H / 64;              // 128-byte swizzle regions per row
+  static constexpr int kRegionBytes = 128 * 128;       // resident tile: 128 rows x 128 bytes
+  static constexpr int kSRegionBytes = STEP * 128;     // streamed tile: STEP rows x 128 bytes
+  static constexpr int kTile = kBM * H * 2;            // resident 128-row tile
+  static constexpr int kSTile = STEP * H * 2;          // streamed STEP-row tile
   static constexpr int kStages = (H == 128) ? 2 : 4;
-  // two resident tiles, then kStages stages of two tiles each
-  static constexpr int kSmem = (2 + 2 * kStages) * kTile + 1024;
-  static constexpr int kTmemS = 0, kTmemP = 128, kTmemA0 = 256, kTmemA1 = 256 + H;
-  static constexpr uint32_t kTmemCols = 512;
-  static constexpr int kThreads = 256;             // 4 control warps + one warpgroup
+  // two resident tiles, then kStages stages of two streamed tiles each
+  static constexpr int kSmem = 2 * kTile + 2 * kStages * kSTile + 1024;
+  static constexpr int kTmemS = 0, kTmemP = STEP, kTmemA0 = 2 * STEP, kTmemA1 = 2 * STEP + H;
+  static constexpr uint32_t kTmemCols = (2 * STEP + 2 * H <= 256) ? 256 : 512;
+  static constexpr int kThreads = 256;                 // 4 control warps + one warpgroup
+  static constexpr int kMinBlocks = (kTmemCols == 256) ? 2 : 1;
 };
 
 __device__ __forceinline__ void perm_coords(int ds, int dn, int db, int s, int n, int b, int& c1, int& c2, int& c3) {
@@ -144,20 +150,20 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   return kBF16 ? pack_bf16x2(lo, hi) : pack_f16x2(lo, hi);
 }
 
-// One 128 x 128 tile of scores and score gradients in TMEM (this thread's lane = one row):
+// One 128 x (32 NCH) tile of scores and score gradients in TMEM (this thread's lane = one row):
 // P = 2^(s scale log2e - L) on admitted entries and dS' = P (dP - delta) (the score scale is
 // applied once to the accumulated dQ / dK instead); P goes over the first 64 columns of S and
 // dS' over the first 64 columns of dP (or of S when P is not wanted), as packed 16-bit pairs.
 // Entry e of the row is admitted when e_lo <= e <= e_hi (full: every entry); -L and -delta
 // come per entry from shared memory (kPerCol) or are the row's own.
-template <bool kBF16, bool kWantP, bool kPerCol>
+template <bool kBF16, bool kWantP, bool kPerCol, int NCH>
 __device__ __forceinline__ void grad_tile(uint32_t tS, uint32_t tdP, float scale_log2, int e_lo, int e_hi,
                                           bool full, float nL_row, float nd_row, const float* nL_col,
                                           const float* nd_col) {
   const f2_t sl2 = f2_pack(scale_log2, scale_log2);
   const f2_t nL_r = f2_pack(nL_row, nL_row), nd_r = f2_pack(nd_row, nd_row);
 #pragma unroll 1
-  for (int c = 0; c < 4; ++c) {
+  for (int c = 0; c < NCH; ++c) {
     uint32_t us[32], ud[32];
     tmem_ld32(tS + c * 32, us);
     tmem_ld32(tdP + c * 32, ud);
@@ -227,11 +233,11 @@ __device__ __forceinline__ void store_row(uint32_t tAcc, bool have, bool valid, 
 constexpr uint64_t kDrainNs = 2000000000ull;
 
 // ------------------------------------------------------------------------- dK, dV
-template <int H, bool kBF16>
-__global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
+template <int H, int STEP, bool kBF16>
+__global__ void __launch_bounds__(BCfg<H, STEP>::kThreads, BCfg<H, STEP>::kMinBlocks)
     bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tg,
                     const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, const BwdArgs a) {
-  using C = BCfg<H>;
+  using C = BCfg<H, STEP>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_kv, bar_sready, bar_pready, bar_acc, bar_stat[2];
@@ -248,12 +254,13 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
   const int64_t len_b = len_of(a, b);
   const int64_t k0 = (int64_t)kt * kBM, k1 = bmin((int64_t)a.T, k0 + kBM) - 1;
 
-  // query tiles that admit some key of this tile: a contiguous range (the bounds grow with i)
-  int qt_lo = a.nq_tiles, qt_hi = -1;
-  for (int qt = 0; qt < a.nq_tiles; ++qt) {
+  // query steps that admit some key of this tile: a contiguous range (the bounds grow with i)
+  const int nqs = (a.S + STEP - 1) / STEP;
+  int qt_lo = nqs, qt_hi = -1;
+  for (int qt = 0; qt < nqs; ++qt) {
     int64_t lo0, hi0, lo1, hi1;
-    key_range(a, len_b, (int64_t)qt * kBM, lo0, hi0);
-    key_range(a, len_b, bmin((int64_t)a.S, (int64_t)qt * kBM + kBM) - 1, lo1, hi1);
+    key_range(a, len_b, (int64_t)qt * STEP, lo0, hi0);
+    key_range(a, len_b, bmin((int64_t)a.S, (int64_t)qt * STEP + STEP) - 1, lo1, hi1);
     const int64_t lo = bmin(lo0, lo1), hi = bmax(hi0, hi1);
     if (hi >= lo && lo <= k1 && hi >= k0) {
       if (qt < qt_lo) qt_lo = qt;
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
     }
   }
   const int nqt = qt_hi >= qt_lo ? qt_hi - qt_lo + 1 : 0;
-  const int n_steps = nqt * a.group;   // step n: query tile qt_lo + n / group, head n % group
+  const int n_steps = nqt * a.group;   // step n: query step qt_lo + n / group, head n % group
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sK = sbase, sV = sbase + C::kTile, sRing = sbase + 2 * C::kTile;
@@ -309,12 +316,12 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
             !mbar_wait_bounded(b_empty(st), ((n / C::kStages) - 1) & 1, abortp, a.wait_ns))
           break;
         const int qt = qt_lo + n / a.group, h = kvh * a.group + n % a.group;
-        const uint32_t sQ = sRing + st * 2 * C::kTile, sG = sQ + C::kTile;
-        mbar_arrive_expect_tx(b_full(st), 2 * C::kTile);
-        perm_coords(a.q_ds, a.q_dn, a.q_db, qt * kBM, h, b, c1, c2, c3);
-        for (int r = 0; r < C::kRegions; ++r) tma_load_4d(sQ + r * C::kRegionBytes, &tq, b_full(st), 64 * r, c1, c2, c3);
-        perm_coords(a.g_ds, a.g_dn, a.g_db, qt * kBM, h, b, c1, c2, c3);
-        for (int r = 0; r < C::kRegions; ++r) tma_load_4d(sG + r * C::kRegionBytes, &tg, b_full(st), 64 * r, c1, c2, c3);
+        const uint32_t sQ = sRing + st * 2 * C::kSTile, sG = sQ + C::kSTile;
+        mbar_arrive_expect_tx(b_full(st), 2 * C::kSTile);
+        perm_coords(a.q_ds, a.q_dn, a.q_db, qt * STEP, h, b, c1, c2, c3);
+        for (int r = 0; r < C::kRegions; ++r) tma_load_4d(sQ + r * C::kSRegionBytes, &tq, b_full(st), 64 * r, c1, c2, c3);
+        perm_coords(a.g_ds, a.g_dn, a.g_db, qt * STEP, h, b, c1, c2, c3);
+        for (int r = 0; r < C::kRegions; ++r) tma_load_4d(sG + r * C::kSRegionBytes, &tg, b_full(st), 64 * r, c1, c2, c3);
       }
       if (n < n_steps || *abortp) {
         // some role gave up: let every copy already issued land before the CTA can exit
@@ -329,7 +336,7 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
   } else if (warp == 1) {
     // ======================================================== MMA issuer
     if (lane == 0 && n_steps > 0) {
-      constexpr uint32_t kIdS = idesc_f16(kBF16, kBM, 128, false);   // M keys, N queries
+      constexpr uint32_t kIdS = idesc_f16(kBF16, kBM, STEP, false);  // M keys, N queries
       constexpr uint32_t kIdA = idesc_f16(kBF16, kBM, H, true);      // M keys, N head dims
       const uint32_t tS = tmem + C::kTmemS, tP = tmem + C::kTmemP;
       const uint32_t tdK = tmem + C::kTmemA0, tdV = tmem + C::kTmemA1;
@@ -340,29 +347,31 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
         const int st = n % C::kStages;
         if (!(ok = mbar_wait_bounded(b_full(st), (n / C::kStages) & 1, abortp, a.wait_ns))) break;
         tc_fence_after();
-        const uint32_t sQ = sRing + st * 2 * C::kTile, sG = sQ + C::kTile;
+        const uint32_t sQ = sRing + st * 2 * C::kSTile, sG = sQ + C::kSTile;
         const uint64_t dQk = desc_sw128(sQ, 16, 1024), dGk = desc_sw128(sG, 16, 1024);
-        const uint64_t dQm = desc_sw128(sQ, C::kRegionBytes, 1024), dGm = desc_sw128(sG, C::kRegionBytes, 1024);
+        const uint64_t dQm = desc_sw128(sQ, C::kSRegionBytes, 1024), dGm = desc_sw128(sG, C::kSRegionBytes, 1024);
         // S^T = K Q^T and dP^T = V dY^T (after the accumulations of step n-1 read P^T / dS^T)
 #pragma unroll
         for (int kk = 0; kk < H / 16; ++kk) {
-          const uint64_t off = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
-          mma_f16_ss(tS, dK + off, dQk + off, kIdS, kk > 0);
+          const uint64_t offa = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
+          const uint64_t offb = (uint64_t)(((kk / 4) * C::kSRegionBytes + (kk % 4) * 32) >> 4);
+          mma_f16_ss(tS, dK + offa, dQk + offb, kIdS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < H / 16; ++kk) {
-          const uint64_t off = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
-          mma_f16_ss(tP, dV + off, dGk + off, kIdS, kk > 0);
+          const uint64_t offa = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
+          const uint64_t offb = (uint64_t)(((kk / 4) * C::kSRegionBytes + (kk % 4) * 32) >> 4);
+          mma_f16_ss(tP, dV + offa, dGk + offb, kIdS, kk > 0);
         }
         mma_commit(b_sready);
         if (!(ok = mbar_wait_bounded(b_pready, n & 1, abortp, a.wait_ns))) break;
         tc_fence_after();
         // dV += P^T dY and dK += dS^T Q: A from TMEM (16 queries = 8 columns per K step)
 #pragma unroll
-        for (int kk = 0; kk < kBM / 16; ++kk)
+        for (int kk = 0; kk < STEP / 16; ++kk)
           mma_f16_ts(tdV, tS + kk * 8, dGm + (uint64_t)((kk * 2048) >> 4), kIdA, (n > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
-        for (int kk = 0; kk < kBM / 16; ++kk)
+        for (int kk = 0; kk < STEP / 16; ++kk)
           mma_f16_ts(tdK, tP + kk * 8, dQm + (uint64_t)((kk * 2048) >> 4), kIdA, (n > 0 || kk > 0) ? 1u : 0u);
         mma_commit(b_empty(st));
       }
@@ -383,14 +392,14 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
     bool ok = true;
     for (int n = 0; n < n_steps && ok; ++n) {
       const int qt = qt_lo + n / a.group, h = kvh * a.group + n % a.group;
-      const int64_t q0 = (int64_t)qt * kBM;
-      // statistics of the tile's 128 query rows into shared memory (row q0 + row), double
+      const int64_t q0 = (int64_t)qt * STEP;
+      // statistics of the step's STEP query rows into shared memory (row q0 + row), double
       // buffered: a thread rewrites buffer n & 1 only after every thread arrived for step n-1,
       // that is after every thread finished reading it in step n-2
       {
         const int64_t i = q0 + row;
         float L = INFINITY, d = 0.f;
-        if (i < a.S) {
+        if (row < STEP && i < a.S) {
           const int64_t idx = ((int64_t)b * a.Nq + h) * a.S + i;
           L = a.lse2[idx];
           d = a.delta[idx];
@@ -403,10 +412,11 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
       }
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_sready, n & 1, abortp, a.wait_ns)))) break;
       tc_fence_after();
-      const int e_lo = (int)bmax(-1, bmin((int64_t)kBM, qlo - q0));
-      const int e_hi = (int)bmax(-1, bmin((int64_t)kBM, qhi - q0));
-      const bool full = __all_sync(0xffffffffu, e_lo <= 0 && e_hi >= kBM - 1);
-      grad_tile<kBF16, true, true>(tS, tP, a.scale_log2, e_lo, e_hi, full, 0.f, 0.f, sh_L[n & 1], sh_d[n & 1]);
+      const int e_lo = (int)bmax(-1, bmin((int64_t)STEP, qlo - q0));
+      const int e_hi = (int)bmax(-1, bmin((int64_t)STEP, qhi - q0));
+      const bool full = __all_sync(0xffffffffu, e_lo <= 0 && e_hi >= STEP - 1);
+      grad_tile<kBF16, true, true, STEP / 32>(tS, tP, a.scale_log2, e_lo, e_hi, full, 0.f, 0.f, sh_L[n & 1],
+                                               sh_d[n & 1]);
       tc_fence_before();
       mbar_arrive(b_pready);
     }
@@ -432,11 +442,11 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
 }
 
 // ------------------------------------------------------------------------- dQ
-template <int H, bool kBF16>
-__global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
+template <int H, int STEP, bool kBF16>
+__global__ void __launch_bounds__(BCfg<H, STEP>::kThreads, BCfg<H, STEP>::kMinBlocks)
     bwd_dq_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tg,
                   const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, const BwdArgs a) {
-  using C = BCfg<H>;
+  using C = BCfg<H, STEP>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   __shared__ __align__(8) uint64_t bar_q, bar_sready, bar_pready, bar_acc;
@@ -456,8 +466,8 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
   key_range(a, len_b, m0, lo0, hi0);
   key_range(a, len_b, m1 - 1, lo1, hi1);
   const int64_t klo = bmax(0, bmin(lo0, lo1)), khi = bmin((int64_t)a.T - 1, bmax(hi0, hi1));
-  const int kt0 = (int)(klo / kBM);
-  const int n_steps = khi >= klo ? (int)(khi / kBM) - kt0 + 1 : 0;
+  const int kt0 = (int)(klo / STEP);
+  const int n_steps = khi >= klo ? (int)(khi / STEP) - kt0 + 1 : 0;   // STEP keys per step
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase, sG = sbase + C::kTile, sRing = sbase + 2 * C::kTile;
@@ -501,12 +511,12 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
         if (n >= C::kStages &&
             !mbar_wait_bounded(b_empty(st), ((n / C::kStages) - 1) & 1, abortp, a.wait_ns))
           break;
-        const uint32_t sK = sRing + st * 2 * C::kTile, sV = sK + C::kTile;
-        mbar_arrive_expect_tx(b_full(st), 2 * C::kTile);
-        perm_coords(a.kv_ds, a.kv_dn, a.kv_db, (kt0 + n) * kBM, kvh, b, c1, c2, c3);
+        const uint32_t sK = sRing + st * 2 * C::kSTile, sV = sK + C::kSTile;
+        mbar_arrive_expect_tx(b_full(st), 2 * C::kSTile);
+        perm_coords(a.kv_ds, a.kv_dn, a.kv_db, (kt0 + n) * STEP, kvh, b, c1, c2, c3);
         for (int r = 0; r < C::kRegions; ++r) {
-          tma_load_4d(sK + r * C::kRegionBytes, &tk, b_full(st), 64 * r, c1, c2, c3);
-          tma_load_4d(sV + r * C::kRegionBytes, &tv, b_full(st), 64 * r, c1, c2, c3);
+          tma_load_4d(sK + r * C::kSRegionBytes, &tk, b_full(st), 64 * r, c1, c2, c3);
+          tma_load_4d(sV + r * C::kSRegionBytes, &tv, b_full(st), 64 * r, c1, c2, c3);
         }
       }
       if (n < n_steps || *abortp) {
@@ -521,7 +531,7 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
   } else if (warp == 1) {
     // ======================================================== MMA issuer
     if (lane == 0 && n_steps > 0) {
-      constexpr uint32_t kIdS = idesc_f16(kBF16, kBM, 128, false);   // M queries, N keys
+      constexpr uint32_t kIdS = idesc_f16(kBF16, kBM, STEP, false);  // M queries, N keys
       constexpr uint32_t kIdA = idesc_f16(kBF16, kBM, H, true);      // M queries, N head dims
       const uint32_t tS = tmem + C::kTmemS, tP = tmem + C::kTmemP, tdQ = tmem + C::kTmemA0;
       const uint64_t dQ = desc_sw128(sQ, 16, 1024), dG = desc_sw128(sG, 16, 1024);
@@ -531,26 +541,28 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
         const int st = n % C::kStages;
         if (!(ok = mbar_wait_bounded(b_full(st), (n / C::kStages) & 1, abortp, a.wait_ns))) break;
         tc_fence_after();
-        const uint32_t sK = sRing + st * 2 * C::kTile, sV = sK + C::kTile;
+        const uint32_t sK = sRing + st * 2 * C::kSTile, sV = sK + C::kSTile;
         const uint64_t dKk = desc_sw128(sK, 16, 1024), dVk = desc_sw128(sV, 16, 1024);
-        const uint64_t dKm = desc_sw128(sK, C::kRegionBytes, 1024);
+        const uint64_t dKm = desc_sw128(sK, C::kSRegionBytes, 1024);
         // S = Q K^T and dP = dY V^T (after dQ of step n-1 read dS)
 #pragma unroll
         for (int kk = 0; kk < H / 16; ++kk) {
-          const uint64_t off = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
-          mma_f16_ss(tS, dQ + off, dKk + off, kIdS, kk > 0);
+          const uint64_t offa = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
+          const uint64_t offb = (uint64_t)(((kk / 4) * C::kSRegionBytes + (kk % 4) * 32) >> 4);
+          mma_f16_ss(tS, dQ + offa, dKk + offb, kIdS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < H / 16; ++kk) {
-          const uint64_t off = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
-          mma_f16_ss(tP, dG + off, dVk + off, kIdS, kk > 0);
+          const uint64_t offa = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
+          const uint64_t offb = (uint64_t)(((kk / 4) * C::kSRegionBytes + (kk % 4) * 32) >> 4);
+          mma_f16_ss(tP, dG + offa, dVk + offb, kIdS, kk > 0);
         }
         mma_commit(b_sready);
         if (!(ok = mbar_wait_bounded(b_pready, n & 1, abortp, a.wait_ns))) break;
         tc_fence_after();
         // dQ += dS K: dS from TMEM (16 keys = 8 columns per K step), K MN-major
 #pragma unroll
-        for (int kk = 0; kk < 128 / 16; ++kk)
+        for (int kk = 0; kk < STEP / 16; ++kk)
           mma_f16_ts(tdQ, tS + kk * 8, dKm + (uint64_t)((kk * 2048) >> 4), kIdA, (n > 0 || kk > 0) ? 1u : 0u);
         mma_commit(b_empty(st));
       }
@@ -578,11 +590,11 @@ __global__ void __launch_bounds__(BCfg<H>::kThreads, 1)
     for (int n = 0; n < n_steps && ok; ++n) {
       if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_sready, n & 1, abortp, a.wait_ns)))) break;
       tc_fence_after();
-      const int64_t key0 = (int64_t)(kt0 + n) * kBM;
-      const int e_lo = (int)bmax(-1, bmin((int64_t)kBM, lo - key0));
-      const int e_hi = (int)bmax(-1, bmin((int64_t)kBM, hi - key0));
-      const bool full = __all_sync(0xffffffffu, e_lo <= 0 && e_hi >= kBM - 1);
-      grad_tile<kBF16, false, false>(tS, tP, a.scale_log2, e_lo, e_hi, full, -L, -d, nullptr, nullptr);
+      const int64_t key0 = (int64_t)(kt0 + n) * STEP;
+      const int e_lo = (int)bmax(-1, bmin((int64_t)STEP, lo - key0));
+      const int e_hi = (int)bmax(-1, bmin((int64_t)STEP, hi - key0));
+      const bool full = __all_sync(0xffffffffu, e_lo <= 0 && e_hi >= STEP - 1);
+      grad_tile<kBF16, false, false, STEP / 32>(tS, tP, a.scale_log2, e_lo, e_hi, full, -L, -d, nullptr, nullptr);
       tc_fence_before();
       mbar_arrive(b_pready);
     }
@@ -611,29 +623,32 @@ uint64_t bwd_wait_ns() {
   return v;
 }
 
-template <int H, bool kBF16>
+// Maps: tq / tg cover Q and dY, tk / tv K and V; the "s" maps have STEP-row boxes (the
+// streamed tiles), the others 128-row boxes (the resident ones).
+template <int H, int STEP, bool kBF16>
 cudaError_t launch_bwd_t(const CUtensorMap& tq, const CUtensorMap& tg, const CUtensorMap& tk, const CUtensorMap& tv,
-                         const BwdArgs& a_kv, const BwdArgs& a_q, cudaStream_t st) {
-  using C = BCfg<H>;
+                         const CUtensorMap& tqs, const CUtensorMap& tgs, const CUtensorMap& tks,
+                         const CUtensorMap& tvs, const BwdArgs& a_kv, const BwdArgs& a_q, cudaStream_t st) {
+  using C = BCfg<H, STEP>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(bwd_dkdv_kernel<H, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    attr_err = cudaFuncSetAttribute(bwd_dkdv_kernel<H, STEP, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(bwd_dq_kernel<H, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+      attr_err = cudaFuncSetAttribute(bwd_dq_kernel<H, STEP, kBF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   });
   if (attr_err != cudaSuccess) return attr_err;
   const int64_t g1 = (int64_t)a_kv.nk_tiles * a_kv.B * a_kv.Nkv;
   const int64_t g2 = (int64_t)a_q.nq_tiles * a_q.B * a_q.Nq;
   if (g1 > 0x7fffffff || g2 > 0x7fffffff) return cudaErrorInvalidValue;
   if (g1 > 0) {
-    bwd_dkdv_kernel<H, kBF16><<<(unsigned)g1, C::kThreads, C::kSmem, st>>>(tq, tg, tk, tv, a_kv);
+    bwd_dkdv_kernel<H, STEP, kBF16><<<(unsigned)g1, C::kThreads, C::kSmem, st>>>(tqs, tgs, tk, tv, a_kv);
     count_launch(1);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   if (g2 > 0) {
-    bwd_dq_kernel<H, kBF16><<<(unsigned)g2, C::kThreads, C::kSmem, st>>>(tq, tg, tk, tv, a_q);
+    bwd_dq_kernel<H, STEP, kBF16><<<(unsigned)g2, C::kThreads, C::kSmem, st>>>(tq, tg, tks, tvs, a_q);
     count_launch(1);
     return cudaGetLastError();
   }
@@ -671,12 +686,18 @@ cudaError_t launch_bwd_tc(const Problem& p, sdpa_dtype dt, const View& dy, const
   a.nk_tiles = (int)((p.T + kBM - 1) / kBM);
   a.wait_ns = bwd_wait_ns();
   if (!tc_encode_fn()) return cudaErrorNotSupported;
-  CUtensorMap tq, tg, tk, tv;
-  int vds, vdn, vdb;
+  // 64-row streamed tiles for H = 64 (two CTAs per SM), 128 rows for H = 128
+  const int step = p.H == 64 ? 64 : 128;
+  CUtensorMap tq, tg, tk, tv, tqs, tgs, tks, tvs;
+  int vds, vdn, vdb, x1, x2, x3;
   if (!tc_make_map(&tq, p.q, dt, p.B, p.Nq, p.S, p.H, &a.q_ds, &a.q_dn, &a.q_db) ||
       !tc_make_map(&tg, dy, dt, p.B, p.Nq, p.S, p.Hv, &a.g_ds, &a.g_dn, &a.g_db) ||
       !tc_make_map(&tk, p.k, dt, p.B, p.Nkv, p.T, p.H, &a.kv_ds, &a.kv_dn, &a.kv_db) ||
-      !tc_make_map(&tv, p.v, dt, p.B, p.Nkv, p.T, p.Hv, &vds, &vdn, &vdb))
+      !tc_make_map(&tv, p.v, dt, p.B, p.Nkv, p.T, p.Hv, &vds, &vdn, &vdb) ||
+      !tc_make_map(&tqs, p.q, dt, p.B, p.Nq, p.S, p.H, &x1, &x2, &x3, step) ||
+      !tc_make_map(&tgs, dy, dt, p.B, p.Nq, p.S, p.Hv, &x1, &x2, &x3, step) ||
+      !tc_make_map(&tks, p.k, dt, p.B, p.Nkv, p.T, p.H, &x1, &x2, &x3, step) ||
+      !tc_make_map(&tvs, p.v, dt, p.B, p.Nkv, p.T, p.Hv, &x1, &x2, &x3, step))
     return cudaErrorInvalidValue;
   if (vds != a.kv_ds || vdn != a.kv_dn || vdb != a.kv_db) return cudaErrorInvalidValue;
   BwdArgs akv = a, aq = a;
@@ -686,10 +707,12 @@ cudaError_t launch_bwd_tc(const Problem& p, sdpa_dtype dt, const View& dy, const
   const bool bf = dt == SDPA_BF16;
   if (p.H == 128) {
     *name = bf ? "bwd_tc_bf16_h128" : "bwd_tc_f16_h128";
-    return bf ? launch_bwd_t<128, true>(tq, tg, tk, tv, akv, aq, st) : launch_bwd_t<128, false>(tq, tg, tk, tv, akv, aq, st);
+    return bf ? launch_bwd_t<128, 128, true>(tq, tg, tk, tv, tqs, tgs, tks, tvs, akv, aq, st)
+              : launch_bwd_t<128, 128, false>(tq, tg, tk, tv, tqs, tgs, tks, tvs, akv, aq, st);
   }
   *name = bf ? "bwd_tc_bf16_h64" : "bwd_tc_f16_h64";
-  return bf ? launch_bwd_t<64, true>(tq, tg, tk, tv, akv, aq, st) : launch_bwd_t<64, false>(tq, tg, tk, tv, akv, aq, st);
+  return bf ? launch_bwd_t<64, 64, true>(tq, tg, tk, tv, tqs, tgs, tks, tvs, akv, aq, st)
+            : launch_bwd_t<64, 64, false>(tq, tg, tk, tv, tqs, tgs, tks, tvs, akv, aq, st);
 }
 
 cudaError_t take_bwd_status(int* status) {

@@ -1004,7 +1004,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // 4-D map over a (B, N, Seq, D) view: dim 0 = D (contiguous); dims 1..3 = the axes in
 // tc_axis_order.  Box: 64 x 128 rows.
 bool make_map(CUtensorMap* map, const View& v, sdpa_dtype dt, int64_t B, int64_t N, int64_t Sq, int D, int* ds,
-              int* dn, int* db) {
+              int* dn, int* db, int box_rows = kBN) {
   auto enc = encode_fn();
   if (!enc) return false;
   const int64_t ext[3] = {Sq, N, B};
@@ -1023,7 +1023,7 @@ bool make_map(CUtensorMap* map, const View& v, sdpa_dtype dt, int64_t B, int64_t
     if (ext[id] == 1) sb = ((prev_end + 15) / 16) * 16;   // never stepped: any legal stride
     strides[k] = (cuuint64_t)sb;
     prev_end = std::max<int64_t>(prev_end, sb * ext[id]);
-    if (id == 0) { box[k + 1] = kBN; *ds = k + 1; }
+    if (id == 0) { box[k + 1] = (cuuint32_t)box_rows; *ds = k + 1; }
     if (id == 1) *dn = k + 1;
     if (id == 2) *db = k + 1;
   }
@@ -1194,8 +1194,8 @@ cudaError_t launch_prefill_tc_stats(const Problem& p, sdpa_dtype dt, float* lse2
 PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() { return encode_fn(); }
 
 bool tc_make_map(CUtensorMap* map, const View& v, sdpa_dtype dt, int64_t B, int64_t N, int64_t Sq, int D, int* ds,
-                 int* dn, int* db) {
-  return make_map(map, v, dt, B, N, Sq, D, ds, dn, db);
+                 int* dn, int* db, int box_rows) {
+  return make_map(map, v, dt, B, N, Sq, D, ds, dn, db, box_rows);
 }
 
 cudaError_t take_prefill_status(int* status) {

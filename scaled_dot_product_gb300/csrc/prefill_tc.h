@@ -20,11 +20,11 @@ void tc_axis_order(const View& v, int64_t B, int64_t N, int64_t S, int order[3])
 bool tc_same_axis_order(const View& k, const View& v, int64_t B, int64_t N, int64_t T);
 
 // Driver entry point of cuTensorMapEncodeTiled (nullptr when unavailable), and the 4-D
-// 16-bit map over a (B, N, Seq, D) view the kernels use (box 64 x 128 rows, 128-byte
+// 16-bit map over a (B, N, Seq, D) view the kernels use (box 64 x box_rows rows, 128-byte
 // swizzle); ds / dn / db receive the map dimension of seq / head / batch.
 PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn();
 bool tc_make_map(CUtensorMap* map, const View& v, sdpa_dtype dt, int64_t B, int64_t N, int64_t Sq, int D, int* ds,
-                 int* dn, int* db);
+                 int* dn, int* db, int box_rows = 128);
 
 // Launches the fused kernel; p.k / p.v must hold all T key rows (P == 0, no kv bias).
 cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, const char** name);
