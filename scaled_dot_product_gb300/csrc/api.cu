@@ -297,8 +297,6 @@ int bwd_check(const sdpa_params* p, const Problem& r, const Rot& rot) {
   if (rot.on) return fail(SDPA_ERR_UNSUPPORTED, "backward: no rotary step");
   if (p->qk_out.data) return fail(SDPA_ERR_UNSUPPORTED, "backward: no qk output");
   if (p->present_k.data) return fail(SDPA_ERR_INVALID, "backward: present outputs are not written");
-  if (p->add_mask.data || p->keep_kind != SDPA_KEEP_NONE || p->len_kind == SDPA_LEN_KEYLEN_I32)
-    return fail(SDPA_ERR_UNSUPPORTED, "backward: interval rules only (no float / bool / filter masks)");
   if (!tc_same_axis_order(r.k, r.v, r.B, r.Nkv, r.T))
     return fail(SDPA_ERR_UNSUPPORTED, "backward: k and v views must walk their axes in the same order");
   return SDPA_OK;

@@ -62,6 +62,8 @@ struct BwdArgs {
   int64_t o1_sb, o1_sh, o1_ss;
   int nq_tiles, nk_tiles;
   uint64_t wait_ns;
+  Rules r;                  // masks: additive, keep (bool / binary), key-padding lengths
+  int has_extra;            // any of them present
 };
 
 // H: head size; STEP: rows of the streamed tiles (the queries of one dK/dV step, the keys of
@@ -94,7 +96,8 @@ __device__ __forceinline__ int64_t bmax(int64_t x, int64_t y) { return x > y ? x
 
 __device__ __forceinline__ int64_t len_of(const BwdArgs& a, int b) {
   if (a.len_kind == SDPA_LEN_NONPAD_I64) return reinterpret_cast<const int64_t*>(a.lens)[b];
-  if (a.len_kind == SDPA_LEN_SEQLENS_K_I32) return reinterpret_cast<const int32_t*>(a.lens)[b];
+  if (a.len_kind == SDPA_LEN_SEQLENS_K_I32 || a.len_kind == SDPA_LEN_KEYLEN_I32)
+    return reinterpret_cast<const int32_t*>(a.lens)[b];
   return 0;
 }
 
@@ -136,6 +139,31 @@ __device__ __forceinline__ void query_range(const BwdArgs& a, int64_t len_b, int
   }
 }
 
+// Additive term of score (i, j) in natural units from the masks: the float mask (-inf past
+// its end), a keep mask (bool: -inf for a dropped key; binary: + mask_filter_value) and
+// MultiHeadAttention key-padding lengths (+ mask_filter_value from the length on).
+__device__ __forceinline__ float extra_term(const Rules& r, int64_t len_b, int b, int h, int64_t i, int64_t j) {
+  float e = 0.f;
+  if (r.add) {
+    if (j >= r.add_T) return -INFINITY;
+    e += load_scalar(r.add, r.add_dtype, b * r.add_sb + h * r.add_sh + i * r.add_ss + j);
+  }
+  if (r.keep_kind != SDPA_KEEP_NONE) {
+    bool keep = false;
+    if (j < r.keep_T) {
+      const int64_t o = b * r.keep_sb + h * r.keep_sh + i * r.keep_ss + j;
+      keep = (r.keep_kind == SDPA_KEEP_BOOL_U8) ? (reinterpret_cast<const uint8_t*>(r.keep)[o] != 0)
+                                                : (reinterpret_cast<const int32_t*>(r.keep)[o] != 0);
+    }
+    if (!keep) {
+      if (r.keep_kind == SDPA_KEEP_BOOL_U8) return -INFINITY;
+      e += r.filter;
+    }
+  }
+  if (r.len_kind == SDPA_LEN_KEYLEN_I32 && j >= len_b) e += r.filter;
+  return e;
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
@@ -156,10 +184,10 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 // dS' over the first 64 columns of dP (or of S when P is not wanted), as packed 16-bit pairs.
 // Entry e of the row is admitted when e_lo <= e <= e_hi (full: every entry); -L and -delta
 // come per entry from shared memory (kPerCol) or are the row's own.
-template <bool kBF16, bool kWantP, bool kPerCol, int NCH>
+template <bool kBF16, bool kWantP, bool kPerCol, int NCH, bool kMask = false, typename F = int>
 __device__ __forceinline__ void grad_tile(uint32_t tS, uint32_t tdP, float scale_log2, int e_lo, int e_hi,
                                           bool full, float nL_row, float nd_row, const float* nL_col,
-                                          const float* nd_col) {
+                                          const float* nd_col, F extra = 0) {
   const f2_t sl2 = f2_pack(scale_log2, scale_log2);
   const f2_t nL_r = f2_pack(nL_row, nL_row), nd_r = f2_pack(nd_row, nd_row);
 #pragma unroll 1
@@ -178,6 +206,12 @@ __device__ __forceinline__ void grad_tile(uint32_t tS, uint32_t tdP, float scale
         const float2 dv = *reinterpret_cast<const float2*>(nd_col + col);
         nL = f2_pack(Lv.x, Lv.y);
         nd = f2_pack(dv.x, dv.y);
+      }
+      if constexpr (kMask) {
+        // the masks' additive terms (natural units) join the exponent's offset
+        float a0, a1;
+        f2_unpack(nL, a0, a1);
+        nL = f2_pack(fmaf(extra(col), kLog2e, a0), fmaf(extra(col + 1), kLog2e, a1));
       }
       float p0, p1;
       f2_unpack(f2_fma(f2_pack(__uint_as_float(us[e]), __uint_as_float(us[e + 1])), sl2, nL), p0, p1);
@@ -415,8 +449,15 @@ __global__ void __launch_bounds__(BCfg<H, STEP>::kThreads, BCfg<H, STEP>::kMinBl
       const int e_lo = (int)bmax(-1, bmin((int64_t)STEP, qlo - q0));
       const int e_hi = (int)bmax(-1, bmin((int64_t)STEP, qhi - q0));
       const bool full = __all_sync(0xffffffffu, e_lo <= 0 && e_hi >= STEP - 1);
-      grad_tile<kBF16, true, true, STEP / 32>(tS, tP, a.scale_log2, e_lo, e_hi, full, 0.f, 0.f, sh_L[n & 1],
-                                               sh_d[n & 1]);
+      if (a.has_extra) {
+        // rows past S (a ragged last step) have L = +inf; their masks are not read
+        auto extra = [&](int col) { return q0 + col < a.S ? extra_term(a.r, len_b, b, h, q0 + col, j) : 0.f; };
+        grad_tile<kBF16, true, true, STEP / 32, true>(tS, tP, a.scale_log2, e_lo, e_hi, full, 0.f, 0.f,
+                                                      sh_L[n & 1], sh_d[n & 1], extra);
+      } else {
+        grad_tile<kBF16, true, true, STEP / 32>(tS, tP, a.scale_log2, e_lo, e_hi, full, 0.f, 0.f, sh_L[n & 1],
+                                                 sh_d[n & 1]);
+      }
       tc_fence_before();
       mbar_arrive(b_pready);
     }
@@ -594,7 +635,13 @@ __global__ void __launch_bounds__(BCfg<H, STEP>::kThreads, BCfg<H, STEP>::kMinBl
       const int e_lo = (int)bmax(-1, bmin((int64_t)STEP, lo - key0));
       const int e_hi = (int)bmax(-1, bmin((int64_t)STEP, hi - key0));
       const bool full = __all_sync(0xffffffffu, e_lo <= 0 && e_hi >= STEP - 1);
-      grad_tile<kBF16, false, false, STEP / 32>(tS, tP, a.scale_log2, e_lo, e_hi, full, -L, -d, nullptr, nullptr);
+      if (a.has_extra) {
+        auto extra = [&](int col) { return valid ? extra_term(a.r, len_b, b, qh, i, key0 + col) : 0.f; };
+        grad_tile<kBF16, false, false, STEP / 32, true>(tS, tP, a.scale_log2, e_lo, e_hi, full, -L, -d, nullptr,
+                                                        nullptr, extra);
+      } else {
+        grad_tile<kBF16, false, false, STEP / 32>(tS, tP, a.scale_log2, e_lo, e_hi, full, -L, -d, nullptr, nullptr);
+      }
       tc_fence_before();
       mbar_arrive(b_pready);
     }
@@ -682,6 +729,8 @@ cudaError_t launch_bwd_tc(const Problem& p, sdpa_dtype dt, const View& dy, const
   a.lens = p.r.lens;
   a.lse2 = lse2;
   a.delta = delta;
+  a.r = p.r;
+  a.has_extra = p.r.add != nullptr || p.r.keep_kind != SDPA_KEEP_NONE || p.r.len_kind == SDPA_LEN_KEYLEN_I32;
   a.nq_tiles = (p.S + kBM - 1) / kBM;
   a.nk_tiles = (int)((p.T + kBM - 1) / kBM);
   a.wait_ns = bwd_wait_ns();

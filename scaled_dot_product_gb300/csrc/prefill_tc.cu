@@ -1073,8 +1073,12 @@ template <int H, bool kBF16>
 cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TcArgs& a,
                      int64_t heads_batches, cudaStream_t st) {
   if (a.lse2_out) {
-    // the backward's statistics pass: interval rules only (the backward rejects the rest)
-    if (a.generic || a.add_fast || a.has_softcap) return cudaErrorInvalidValue;
+    // the backward's statistics pass, in the rule mode of the problem (no softcap: the
+    // backward rejects it)
+    if (a.has_softcap) return cudaErrorInvalidValue;
+    if (a.generic) return launch_mode<H, kBF16, kGeneric, 2, 1, true>(tq, tk, tv, a, heads_batches, st);
+    if (a.add_fast) return launch_mode<H, kBF16, kAddMask, 2, 1, true>(tq, tk, tv, a, heads_batches, st);
+    if (a.keep_fast) return launch_mode<H, kBF16, kKeep, 1, 1, true>(tq, tk, tv, a, heads_batches, st);
     return launch_mode<H, kBF16, kPlain, 1, 1, true>(tq, tk, tv, a, heads_batches, st);
   }
   if (a.generic) return launch_mode<H, kBF16, kGeneric, 2, 1>(tq, tk, tv, a, heads_batches, st);

@@ -32,7 +32,7 @@ cudaError_t launch_prefill_tc(const Problem& p, sdpa_dtype dt, cudaStream_t st, 
 // The same kernel as the statistics pass of the backward: per query row (index
 // (b * Nq + h) * S + i) the log2-sum-exp of the scores in units of q.k * scale * log2(e)
 // (+inf for a row with nothing admitted) and delta = dY . O, O the normalised output in fp32.
-// y is written only when p.y.p is set.  Interval rules and sink only (no softcap, no masks).
+// y is written only when p.y.p is set.  Any rule set but softcap.
 cudaError_t launch_prefill_tc_stats(const Problem& p, sdpa_dtype dt, float* lse2, float* delta, const View* dy,
                                     cudaStream_t st, const char** name);
 

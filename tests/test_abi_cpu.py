@@ -288,12 +288,16 @@ def test_backward_subset_validates():
     (dict(H=96, Hv=96), "head size"),
     (dict(H=64, Hv=128), "H != Hv"),
     (dict(P=5), "past rows"),
-    (dict(keep_mask=torch.ones(1, 1, 8, 8, dtype=torch.uint8), keep_kind="bool"), "bool mask"),
-    (dict(add_mask=torch.zeros(1, 1, 8, 8, dtype=torch.bfloat16)), "float mask"),
-    (dict(lens=torch.tensor([3, 8], dtype=torch.int32), len_kind="keylen"), "key-padding lengths"),
+    (dict(k_bias=torch.zeros(128, dtype=torch.bfloat16)), "projection bias"),
 ])
 def test_backward_rejects_outside_its_subset(kw, why):
     assert code(base(**kw), sdpa.SDPA_OP_BWD) == sdpa.SDPA_ERR_UNSUPPORTED, why
+
+
+def test_backward_takes_masks_and_key_lengths():
+    assert code(base(keep_mask=torch.ones(1, 1, 8, 8, dtype=torch.uint8), keep_kind="bool"), sdpa.SDPA_OP_BWD) == sdpa.SDPA_OK
+    assert code(base(add_mask=torch.zeros(1, 1, 8, 8, dtype=torch.bfloat16)), sdpa.SDPA_OP_BWD) == sdpa.SDPA_OK
+    assert code(base(lens=torch.tensor([3, 8], dtype=torch.int32), len_kind="keylen"), sdpa.SDPA_OP_BWD) == sdpa.SDPA_OK
 
 
 def test_backward_rejects_present_outputs():

@@ -118,3 +118,25 @@ def test_backward_full_size_gqa_key_gradient_sums_to_zero_without_sink():
     assert torch.isfinite(dkf).all()
     assert (col.abs() <= 0.02 * mag + 1e-3).all(), float((col.abs() / (mag + 1e-6)).max())
     assert dq.abs().sum() > 0 and dv.abs().sum() > 0
+
+
+MASK_CASES = [
+    dict(name="addmask_bf16_h64", dtype=torch.bfloat16, B=2, Nq=4, Nkv=2, S=150, L=210, H=64,
+         add_mask="float", add_mask_shape=(2, 1, 150, 210), add_mask_range=(-2.0, 1.0), causal="lower_right"),
+    dict(name="addmask_short_f16_h128", dtype=torch.float16, B=1, Nq=2, S=130, L=200, H=128,
+         add_mask="float", add_mask_shape=(1, 2, 130, 190), add_mask_range=(-1.0, 0.5)),
+    dict(name="bool_mask_bf16_h64", dtype=torch.bfloat16, B=2, Nq=2, S=140, L=140, H=64,
+         keep_kind="bool", keep_mask_shape=(2, 1, 140, 140), causal="upper_left"),
+    dict(name="filter_keylen_f16_h64", dtype=torch.float16, B=2, Nq=4, Nkv=1, S=100, L=260, H=64,
+         keep_kind="filter", keep_mask_shape=(2, 1, 1, 260), len_kind="keylen", len_range=(30, 260), sink=True),
+    dict(name="keylen_bf16_h128", dtype=torch.bfloat16, B=2, Nq=2, S=200, L=200, H=128, causal="lower_right",
+         len_kind="keylen", len_range=(50, 200)),
+]
+
+
+@pytest.mark.parametrize("kw", MASK_CASES, ids=[c["name"] for c in MASK_CASES])
+def test_backward_with_masks_matches_oracle(kw):
+    kw = dict(kw)
+    name = kw.pop("name")
+    case = make_case(name, seed=1300 + len(name), keep_density=0.8, **kw)
+    compare(case, draw_dy(case, seed=1400 + len(name)))
