@@ -217,14 +217,16 @@ SDPA_API int sdpa_attn_decode_static(const sdpa_params* p, sdpa_stream_t stream)
  *     dP = dY V^T,  dS = P (dP - rowsum(P dP)) scale,  dQ = dS K,  dK = dS^T Q,  dV = P^T dY,
  * the query heads of a group summed onto their kv head, every output rounded once to dtype.
  * p describes the forward problem exactly as for sdpa_attn_fwd (p->y may be absent and is not
- * written).  dy: (B, Nq, S, Hv) upstream gradient; outputs dq (B, Nq, S, H), dk (B, Nkv, L, H),
- * dv (B, Nkv, L, Hv), all views of dtype elements, written in full (zeros where no score
- * depends on them).  workspace: sdpa_workspace_size(p, SDPA_OP_BWD) bytes (two fp32 values per
- * query row), 256-byte aligned.
- * Subset: float16 / bfloat16, H == Hv in {64, 128}, P == 0, no projection biases, no rotary,
- * no qk output, no present outputs; rules: causal (either alignment), window, nonpad_kv_seqlen
- * or seqlens_k lengths, head_sink.  softcap > 0 returns SDPA_ERR_UNSUPPORTED (the gradient
- * graph has no softcap), as do float / bool / filter masks and key-padding lengths.
+ * written).  dy: (B, Nq, S, Hv) upstream gradient; outputs dq (B, Nq, S, H), dk (B, Nkv, P+L, H),
+ * dv (B, Nkv, P+L, Hv): gradients with respect to the rows the scores see (Q plus its projection
+ * bias; the P past rows followed by the L new rows plus their biases), all views of dtype
+ * elements, written in full (zeros where no score depends on them).  workspace:
+ * sdpa_workspace_size(p, SDPA_OP_BWD) bytes (two fp32 values per query row, plus copies of
+ * the biased Q and of the T key / value rows when there are biases or past rows), 256-byte
+ * aligned.
+ * Subset: float16 / bfloat16, H == Hv in {64, 128}, no rotary, no qk output, no present
+ * outputs; every mask and length rule of sdpa_attn_fwd and head_sink.  softcap > 0 returns
+ * SDPA_ERR_UNSUPPORTED (the gradient graph has no softcap).
  * Alignment and aliasing rules as for sdpa_attn_fwd; outputs overlap no input. */
 SDPA_API int sdpa_attn_bwd(const sdpa_params* p, sdpa_view dy, sdpa_view dq, sdpa_view dk, sdpa_view dv,
                            void* workspace, size_t workspace_bytes, sdpa_stream_t stream);

@@ -283,28 +283,44 @@ size_t fwd_workspace(const Problem& r, sdpa_dtype dt) {
 
 size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
+// Past rows or k / v projection biases: the backward works on contiguous copies of the T key
+// and value rows the scores see (past rows first, biases added), as the forward does.
+bool bwd_materialise_kv(const Problem& r) { return r.P > 0 || r.k_bias || r.v_bias; }
+
 // The backward's subset: the GroupQueryAttention gradient graph has no softcap, and this
-// library's kernels take 16-bit types, H == Hv in {64, 128}, no past rows, no projection
-// biases, no rotary step and the interval rules only (causal, window, nonpad / seqlens_k
-// lengths) plus the sink.
+// library's kernels take 16-bit types, H == Hv in {64, 128} and no rotary step.
 int bwd_check(const sdpa_params* p, const Problem& r, const Rot& rot) {
   const sdpa_dtype dt = (sdpa_dtype)p->dtype;
   if (p->softcap > 0.f) return fail(SDPA_ERR_UNSUPPORTED, "the backward has no softcap derivative");
   if (dt == SDPA_F32) return fail(SDPA_ERR_UNSUPPORTED, "backward: float16 / bfloat16 only");
   if (!bwd_tc_supported(r, dt)) return fail(SDPA_ERR_UNSUPPORTED, "backward: H == Hv in {64, 128} only");
-  if (r.P > 0) return fail(SDPA_ERR_UNSUPPORTED, "backward: no past rows (P=%d)", r.P);
-  if (r.q_bias || r.k_bias || r.v_bias) return fail(SDPA_ERR_UNSUPPORTED, "backward: no projection biases");
   if (rot.on) return fail(SDPA_ERR_UNSUPPORTED, "backward: no rotary step");
   if (p->qk_out.data) return fail(SDPA_ERR_UNSUPPORTED, "backward: no qk output");
   if (p->present_k.data) return fail(SDPA_ERR_INVALID, "backward: present outputs are not written");
-  if (!tc_same_axis_order(r.k, r.v, r.B, r.Nkv, r.T))
+  if (!bwd_materialise_kv(r) && !tc_same_axis_order(r.k, r.v, r.B, r.Nkv, r.T))
     return fail(SDPA_ERR_UNSUPPORTED, "backward: k and v views must walk their axes in the same order");
   return SDPA_OK;
 }
 
-size_t bwd_workspace(const Problem& r) {
-  return 2 * align256((size_t)r.B * r.Nq * (size_t)r.S * sizeof(float));
+// Backward workspace: log2-sum-exp and delta per query row, then Q + q_bias when there is a
+// q bias, then the key and value rows the scores see when they must be materialised.
+struct BwdWs {
+  size_t lse2 = 0, delta = 0, q = 0, k = 0, v = 0, total = 0;
+};
+BwdWs bwd_layout(const Problem& r, sdpa_dtype dt) {
+  BwdWs w;
+  const size_t stat = align256((size_t)r.B * r.Nq * (size_t)r.S * sizeof(float));
+  w.lse2 = 0;
+  w.delta = stat;
+  w.total = 2 * stat;
+  if (r.q_bias) { w.q = w.total; w.total += align256((size_t)r.B * r.Nq * (size_t)r.S * r.H * esize(dt)); }
+  if (bwd_materialise_kv(r)) {
+    w.k = w.total; w.total += align256((size_t)r.B * r.Nkv * (size_t)r.T * r.H * esize(dt));
+    w.v = w.total; w.total += align256((size_t)r.B * r.Nkv * (size_t)r.T * r.Hv * esize(dt));
+  }
+  return w;
 }
+size_t bwd_workspace(const Problem& r, sdpa_dtype dt) { return bwd_layout(r, dt).total; }
 
 // Bytes of workspace for the rotated copies of Q and of the new K rows; 0 without rotary.
 size_t rot_workspace(const Problem& r, const Rot& rot, sdpa_dtype dt) {
@@ -395,7 +411,7 @@ size_t sdpa_workspace_size(const sdpa_params* p, int op) {
   const sdpa_dtype dt = (sdpa_dtype)p->dtype;
   const size_t pre = rot_workspace(r, rot, dt);
   if (op == SDPA_OP_DECODE) return pre + plan_decode(r.B, r.Nq, r.Nkv, r.S, r.T, r.Hv).ws_bytes;
-  if (op == SDPA_OP_BWD) return bwd_check(p, r, rot) == SDPA_OK ? bwd_workspace(r) : 0;
+  if (op == SDPA_OP_BWD) return bwd_check(p, r, rot) == SDPA_OK ? bwd_workspace(r, (sdpa_dtype)p->dtype) : 0;
   return pre + fwd_workspace(after_rotary(r, rot, dt, nullptr), dt);
 }
 
@@ -617,31 +633,56 @@ int sdpa_attn_bwd(const sdpa_params* p, sdpa_view dy, sdpa_view dq, sdpa_view dk
   if ((rc = check_view(dv, "dv", dt, r.B, r.Nkv, r.T, r.Hv, true, false, &edv))) return rc;
   for (const sdpa_view* v : {&dy, &dq, &dk, &dv})
     if ((rc = check_aligned_view(*v, v == &dy ? "dy" : v == &dq ? "dq" : v == &dk ? "dk" : "dv", dt))) return rc;
-  Extent eq, ek, ev;
+  Extent eq, ek, ev, epk, epv;
   check_view(p->q, "q", dt, r.B, r.Nq, r.S, r.H, true, false, &eq);
   check_view(p->k, "k", dt, r.B, r.Nkv, r.L, r.H, true, false, &ek);
   check_view(p->v, "v", dt, r.B, r.Nkv, r.L, r.Hv, true, false, &ev);
-  const Extent ins[] = {eq, ek, ev, edy, flat(p->head_sink, (size_t)r.Nq * esize(dt), "head_sink"),
-                        flat(p->lens, (size_t)r.B * (p->len_kind == SDPA_LEN_NONPAD_I64 ? 8 : 4), "lens")};
+  check_view(p->past_k, "past_k", dt, r.B, r.Nkv, r.P, r.H, r.P > 0, false, &epk);
+  check_view(p->past_v, "past_v", dt, r.B, r.Nkv, r.P, r.Hv, r.P > 0, false, &epv);
+  const Extent ins[] = {eq, ek, ev, epk, epv, edy, flat(p->head_sink, (size_t)r.Nq * esize(dt), "head_sink"),
+                        flat(p->lens, (size_t)r.B * (p->len_kind == SDPA_LEN_NONPAD_I64 ? 8 : 4), "lens"),
+                        flat(p->q_bias, (size_t)r.Nq * r.H * esize(dt), "q_bias"),
+                        flat(p->k_bias, (size_t)r.Nkv * r.H * esize(dt), "k_bias"),
+                        flat(p->v_bias, (size_t)r.Nkv * r.Hv * esize(dt), "v_bias")};
   for (const Extent& o : {edq, edk, edv})
     for (const Extent& in : ins)
       if (overlap(o, in)) return fail(SDPA_ERR_ALIAS, "output %s overlaps input %s", o.name, in.name);
   if (overlap(edq, edk) || overlap(edq, edv) || overlap(edk, edv))
     return fail(SDPA_ERR_ALIAS, "outputs dq / dk / dv overlap");
-  const size_t need = bwd_workspace(r);
+  const BwdWs wl = bwd_layout(r, (sdpa_dtype)dt);
+  const size_t need = wl.total;
   if (need && (!workspace || workspace_bytes < need))
     return fail(SDPA_ERR_WORKSPACE, "workspace of %zu bytes needed, %zu given", need, workspace_bytes);
   if (need && ((uintptr_t)workspace & 255u)) return fail(SDPA_ERR_ALIGNMENT, "workspace not 256-byte aligned");
-  if (need && overlap(flat(workspace, need, "workspace"), edq))
-    return fail(SDPA_ERR_ALIAS, "workspace overlaps dq");
+  for (const Extent& o : {edq, edk, edv})
+    if (need && overlap(flat(workspace, need, "workspace"), o)) return fail(SDPA_ERR_ALIAS, "workspace overlaps an output");
   g_error.clear();
   if ((int64_t)r.B * r.Nq * r.S == 0 && (int64_t)r.B * r.Nkv * r.T == 0) return SDPA_OK;
   auto cv = [](const sdpa_view& v) { return View{v.data, v.stride_b, v.stride_n, v.stride_s}; };
-  float* lse2 = reinterpret_cast<float*>(workspace);
-  float* delta = reinterpret_cast<float*>(reinterpret_cast<char*>(workspace) + need / 2);
+  char* ws = reinterpret_cast<char*>(workspace);
+  float* lse2 = reinterpret_cast<float*>(ws + wl.lse2);
+  float* delta = reinterpret_cast<float*>(ws + wl.delta);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  // the rows the scores see: Q + q_bias, and concat(past, new + bias) for K and V
+  Problem b = r;
+  cudaError_t e = cudaSuccess;
+  if (r.q_bias) {
+    const View qm{ws + wl.q, (int64_t)r.Nq * r.S * r.H, (int64_t)r.S * r.H, r.H};
+    e = launch_kv_concat((sdpa_dtype)dt, r.B, r.Nq, 0, r.S, r.H, View{}, r.q, r.q_bias, qm, st);
+    b.q = qm;
+    b.q_bias = nullptr;
+  }
+  if (e == cudaSuccess && bwd_materialise_kv(r)) {
+    const View km{ws + wl.k, (int64_t)r.Nkv * r.T * r.H, r.T * r.H, r.H};
+    const View vm{ws + wl.v, (int64_t)r.Nkv * r.T * r.Hv, r.T * r.Hv, r.Hv};
+    e = launch_kv_concat((sdpa_dtype)dt, r.B, r.Nkv, r.P, r.L, r.H, r.past_k, r.k, r.k_bias, km, st);
+    if (e == cudaSuccess) e = launch_kv_concat((sdpa_dtype)dt, r.B, r.Nkv, r.P, r.L, r.Hv, r.past_v, r.v, r.v_bias, vm, st);
+    b.k = km; b.v = vm; b.P = 0; b.L = (int)r.T; b.k_bias = nullptr; b.v_bias = nullptr;
+    b.past_k = View{}; b.past_v = View{};
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "backward: materialising the scored rows");
   const char* name = "";
-  cudaError_t e = launch_bwd_tc(r, (sdpa_dtype)dt, cv(dy), cv(dq), cv(dk), cv(dv), lse2, delta,
-                                reinterpret_cast<cudaStream_t>(stream), &name);
+  e = launch_bwd_tc(b, (sdpa_dtype)dt, cv(dy), cv(dq), cv(dk), cv(dv), lse2, delta, st, &name);
   if (e != cudaSuccess) return cuda_fail(e, "backward launch");
   g_kernel = name;
   return SDPA_OK;

@@ -288,15 +288,18 @@ def sdpa_attn_decode_static(q, k, v, *, y=None, stream=None, **kw) -> torch.Tens
 def sdpa_attn_bwd(q, k, v, dy, *, dq=None, dk=None, dv=None, workspace=None, stream=None, **kw):
     """Backward over 4-D (B, N, S, D) CUDA views: returns (dq, dk, dv) for the upstream
     gradient dy (B, Nq, S, Hv).  Keyword arguments describe the forward problem as for
-    sdpa_attn_fwd (head_sink, scale, causal, window, lens / len_kind)."""
+    sdpa_attn_fwd (past_k / past_v, projection biases, masks, lengths, head_sink, scale,
+    causal, window).  dk and dv cover the P past rows followed by the L new rows."""
     B, Nq, S, H = q.shape
     Nkv, L, Hv = k.shape[1], k.shape[2], v.shape[3]
+    past_k = kw.get("past_k")
+    T = L + (0 if past_k is None else past_k.shape[2])
     if dq is None:
         dq = torch.empty(B, Nq, S, H, dtype=q.dtype, device=q.device)
     if dk is None:
-        dk = torch.empty(B, Nkv, L, H, dtype=q.dtype, device=q.device)
+        dk = torch.empty(B, Nkv, T, H, dtype=q.dtype, device=q.device)
     if dv is None:
-        dv = torch.empty(B, Nkv, L, Hv, dtype=q.dtype, device=q.device)
+        dv = torch.empty(B, Nkv, T, Hv, dtype=q.dtype, device=q.device)
     params, keep = make_params(q, k, v, **kw)
     ws, nbytes = _workspace(params, SDPA_OP_BWD, workspace, q.device)
     _check(lib().sdpa_attn_bwd(ctypes.byref(params), _view(dy, keep), _view(dq, keep), _view(dk, keep),

@@ -287,8 +287,6 @@ def test_backward_subset_validates():
     (dict(dtype=torch.float32, H=64, Hv=64), "f32"),
     (dict(H=96, Hv=96), "head size"),
     (dict(H=64, Hv=128), "H != Hv"),
-    (dict(P=5), "past rows"),
-    (dict(k_bias=torch.zeros(128, dtype=torch.bfloat16)), "projection bias"),
 ])
 def test_backward_rejects_outside_its_subset(kw, why):
     assert code(base(**kw), sdpa.SDPA_OP_BWD) == sdpa.SDPA_ERR_UNSUPPORTED, why
@@ -298,6 +296,12 @@ def test_backward_takes_masks_and_key_lengths():
     assert code(base(keep_mask=torch.ones(1, 1, 8, 8, dtype=torch.uint8), keep_kind="bool"), sdpa.SDPA_OP_BWD) == sdpa.SDPA_OK
     assert code(base(add_mask=torch.zeros(1, 1, 8, 8, dtype=torch.bfloat16)), sdpa.SDPA_OP_BWD) == sdpa.SDPA_OK
     assert code(base(lens=torch.tensor([3, 8], dtype=torch.int32), len_kind="keylen"), sdpa.SDPA_OP_BWD) == sdpa.SDPA_OK
+
+
+def test_backward_takes_past_rows_and_projection_biases():
+    assert code(base(P=5), sdpa.SDPA_OP_BWD) == sdpa.SDPA_OK
+    assert code(base(q_bias=torch.zeros(4 * 64, dtype=torch.bfloat16), k_bias=torch.zeros(2 * 64, dtype=torch.bfloat16),
+                     v_bias=torch.zeros(2 * 64, dtype=torch.bfloat16)), sdpa.SDPA_OP_BWD) == sdpa.SDPA_OK
 
 
 def test_backward_rejects_present_outputs():
@@ -311,6 +315,17 @@ def test_backward_workspace_is_two_floats_per_query_row():
     assert sdpa.sdpa_workspace_size(params, sdpa.SDPA_OP_BWD) == 2 * ((3 * 4 * 100 * 4 + 255) // 256 * 256)
     params, _keep = base(softcap=5.0)
     assert sdpa.sdpa_workspace_size(params, sdpa.SDPA_OP_BWD) == 0
+
+
+def test_backward_workspace_holds_the_materialised_rows():
+    """Past rows or k / v biases add contiguous copies of the T key and value rows; a q bias
+    adds a copy of the biased query."""
+    a = lambda n: (n + 255) // 256 * 256
+    stats = 2 * a(2 * 4 * 8 * 4)
+    params, _keep = base(P=5)
+    assert sdpa.sdpa_workspace_size(params, sdpa.SDPA_OP_BWD) == stats + 2 * a(2 * 2 * 13 * 64 * 2)
+    params, _keep = base(q_bias=torch.zeros(4 * 64, dtype=torch.bfloat16))
+    assert sdpa.sdpa_workspace_size(params, sdpa.SDPA_OP_BWD) == stats + a(2 * 4 * 8 * 64 * 2)
 
 
 def test_backward_gradient_alias_is_rejected_before_launch():

@@ -140,3 +140,25 @@ def test_backward_with_masks_matches_oracle(kw):
     name = kw.pop("name")
     case = make_case(name, seed=1300 + len(name), keep_density=0.8, **kw)
     compare(case, draw_dy(case, seed=1400 + len(name)))
+
+
+PAST_BIAS_CASES = [
+    dict(name="past_rows_causal_bf16_h64", dtype=torch.bfloat16, B=2, Nq=4, Nkv=2, S=150, L=150, P=90, H=64,
+         causal="lower_right"),
+    dict(name="past_rows_seqlens_k_f16_h128", dtype=torch.float16, B=2, Nq=2, Nkv=1, S=70, L=70, P=200, H=128,
+         causal="lower_right", len_kind="seqlens_k", len_range=(150, 269), sink=True),
+    dict(name="mha_qkv_bias_bf16_h64", dtype=torch.bfloat16, B=2, Nq=4, S=140, L=180, H=64, q_layout="bsnh",
+         kv_layout="bsnh", qkv_bias="qkv", proj_bias_std=0.3),
+    dict(name="mha_q_bias_past_f16_h64", dtype=torch.float16, B=1, Nq=2, S=130, L=130, P=60, H=64, qkv_bias="q",
+         proj_bias_std=0.3, causal="lower_right"),
+]
+
+
+@pytest.mark.parametrize("kw", PAST_BIAS_CASES, ids=[c["name"] for c in PAST_BIAS_CASES])
+def test_backward_with_past_rows_and_biases_matches_oracle(kw):
+    """dK / dV cover the past rows followed by the new ones; the biases shift the rows the
+    scores see, so the gradients are taken at the biased rows."""
+    kw = dict(kw)
+    name = kw.pop("name")
+    case = make_case(name, seed=1500 + len(name), **kw)
+    compare(case, draw_dy(case, seed=1600 + len(name)))

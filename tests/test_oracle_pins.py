@@ -675,6 +675,28 @@ def test_backward_with_window_sink_and_lower_right_past_equals_autograd_of_the_d
     np.testing.assert_allclose(dv, vt.grad.numpy(), atol=1e-12)
 
 
+def test_backward_with_projection_biases_equals_autograd_of_the_biased_rows():
+    """MultiHeadAttention's projection-bias segments shift Q and the new K / V rows (never
+    the past rows); the gradients with respect to the rows the scores see are those of
+    torch's attention on the shifted rows, past rows first."""
+    B, N, S, L, P, H = 2, 3, 5, 4, 3, 8
+    q, k, v = rnd(B, N, S, H, seed=140), rnd(B, N, L, H, seed=141), rnd(B, N, L, H, seed=142)
+    pk, pv = rnd(B, N, P, H, seed=143), rnd(B, N, P, H, seed=144)
+    bq, bk, bv = rnd(N * H, seed=145), rnd(N * H, seed=146), rnd(N * H, seed=147)
+    dy = rnd(B, N, S, H, seed=148)
+    dq, dk, dv = oracle.backward(Problem(q=q, k=k, v=v, past_k=pk, past_v=pv, q_bias=bq, k_bias=bk, v_bias=bv,
+                                         causal=oracle.CAUSAL_LOWER_RIGHT), dy)
+    qs = q + bq.view(1, N, 1, H)
+    ks = torch.cat([pk, k + bk.view(1, N, 1, H)], 2)
+    vs = torch.cat([pv, v + bv.view(1, N, 1, H)], 2)
+    T = P + L
+    keep = torch.arange(T).view(1, T) <= (T - S + torch.arange(S)).view(S, 1)
+    wq, wk, wv = _torch_grads(qs, ks, vs, dy, attn_mask=keep)
+    assert dk.shape == (B, N, T, H) and dv.shape == (B, N, T, H)
+    for got, want in ((dq, wq), (dk, wk), (dv, wv)):
+        np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
 def test_backward_matches_central_differences_of_the_forward():
     """d(sum dY * Y)/dx from the oracle backward against central differences of the oracle
     forward, with GQA, an additive mask, key lengths (filter), a boolean mask and a sink."""
