@@ -76,17 +76,24 @@ __device__ __forceinline__ float tanh_poly(float u) {
   return fmaf(w, q, u);
 }
 
-template <int H, int kQT>
+template <int H, int kQT, bool kMaskStage = false>
 struct Cfg {
   static constexpr int kRegions = H / 64;              // 128-byte swizzle regions per row
   static constexpr int kRegionBytes = 128 * 128;       // 128 rows x 128 bytes
   static constexpr int kQTile = kBM * H * 2;
   static constexpr int kKVTile = kBN * H * 2;
-  // ring depth: fill the shared memory one CTA (two tiles) or half of it (one tile) may use
-  static constexpr int kStages = (kQT == 2) ? ((H == 128) ? 4 : 10) : ((H == 128) ? 2 : 5);
+  // ring depth: fill the shared memory one CTA (two tiles) or half of it (one tile) may use;
+  // a staged additive mask takes 8 KB per softmax warp out of it
+  static constexpr int kStages = kMaskStage ? ((H == 128) ? 3 : 7)
+                                            : ((kQT == 2) ? ((H == 128) ? 4 : 10) : ((H == 128) ? 2 : 5));
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQT * kQTile;
-  static constexpr int kSmem = kKVOff + kStages * kKVTile + 1024;   // + alignment slack
+  // additive-mask staging: per softmax warp its 32 rows x 128 16-bit columns, 16-byte chunks
+  // of row r swizzled by r mod 16
+  static constexpr int kMaskWarpBytes = 32 * kBN * 2;
+  static constexpr int kMaskOff = kKVOff + kStages * kKVTile;
+  static constexpr int kMaskBytes = kMaskStage ? 4 * kQT * kMaskWarpBytes : 0;
+  static constexpr int kSmem = kMaskOff + kMaskBytes + 1024;   // + alignment slack
   // Tensor memory: S_X (128 columns each), O_X (H columns each) and P_X (16-bit, two per
   // column: 64 columns).  With H = 128 there is no room for P: P_X overwrites the first 64
   // columns of S_X once S_X is in registers.
@@ -109,6 +116,7 @@ struct TcArgs {
   int generic;                                      // per-element rules beyond the structural ones
   int add_fast;                                     // additive mask only: vectorised path
   int add_vec;                                      // bytes per mask load (2, 4, 8 or 16)
+  int add_stage;                                    // mask tiles staged through shared memory
   int keep_fast;                                    // keep mask / key-length filter, no float mask
   int keep_vec;                                     // keep-mask rows allow 16-byte loads
   float filter_raw;                                 // mask_filter_value in units of raw q.k
@@ -204,43 +212,68 @@ __device__ __forceinline__ void load_mask32(const void* row, int dtype, int k0, 
 
 // Mask values of keys [k0, k0 + 128) of one row, as 64 packed 16-bit pairs in the mask's
 // own type (element 2c in the low half of word c).  Keys >= T_mask read -inf.
+// Mask values of columns c0 .. c0+7 of one 16-bit mask row into w[4] (elements 2v, 2v+1 in
+// w[v]): the widest loads the row alignment vec allows, -inf past the mask's T_mask columns.
 template <typename M>
-__device__ __forceinline__ void prefetch_mask128(const M* row, int k0, int64_t T_mask, int vec_bytes,
-                                                 uint32_t* raw) {
+__device__ __forceinline__ void load_mask_chunk(const M* row, int c0, int64_t T_mask, int vec, uint32_t* w) {
   static_assert(sizeof(M) == 2, "16-bit masks");
-  if ((int64_t)k0 + 128 <= T_mask) {
-    const M* p = row + k0;
-    if (vec_bytes >= 16) {
+  const unsigned short* h = reinterpret_cast<const unsigned short*>(row);
+  if ((int64_t)c0 + 8 <= T_mask) {
+    if (vec >= 16) {
+      const uint4 u = __ldg(reinterpret_cast<const uint4*>(h + c0));
+      w[0] = u.x; w[1] = u.y; w[2] = u.z; w[3] = u.w;
+    } else if (vec >= 8) {
+      const uint2 u0 = __ldg(reinterpret_cast<const uint2*>(h + c0)), u1 = __ldg(reinterpret_cast<const uint2*>(h + c0 + 4));
+      w[0] = u0.x; w[1] = u0.y; w[2] = u1.x; w[3] = u1.y;
+    } else if (vec >= 4) {
 #pragma unroll
-      for (int v = 0; v < 16; ++v) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + v);
-        raw[4 * v] = u.x; raw[4 * v + 1] = u.y; raw[4 * v + 2] = u.z; raw[4 * v + 3] = u.w;
-      }
-    } else if (vec_bytes >= 8) {
-#pragma unroll
-      for (int v = 0; v < 32; ++v) {
-        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p) + v);
-        raw[2 * v] = u.x; raw[2 * v + 1] = u.y;
-      }
-    } else if (vec_bytes >= 4) {
-#pragma unroll
-      for (int v = 0; v < 64; ++v) raw[v] = __ldg(reinterpret_cast<const uint32_t*>(p) + v);
+      for (int v = 0; v < 4; ++v) w[v] = __ldg(reinterpret_cast<const uint32_t*>(h + c0) + v);
     } else {
-      const unsigned short* h = reinterpret_cast<const unsigned short*>(p);
 #pragma unroll
-      for (int v = 0; v < 64; ++v) raw[v] = (uint32_t)__ldg(h + 2 * v) | ((uint32_t)__ldg(h + 2 * v + 1) << 16);
+      for (int v = 0; v < 4; ++v) w[v] = (uint32_t)__ldg(h + c0 + 2 * v) | ((uint32_t)__ldg(h + c0 + 2 * v + 1) << 16);
     }
   } else {
-    const unsigned short ninf = sizeof(M) == 2 && std::is_same<M, __half>::value ? 0xFC00u : 0xFF80u;
-    const unsigned short* h = reinterpret_cast<const unsigned short*>(row);
+    const unsigned short ninf = std::is_same<M, __half>::value ? 0xFC00u : 0xFF80u;
 #pragma unroll
-    for (int v = 0; v < 64; ++v) {
-      const int64_t c0 = (int64_t)k0 + 2 * v, c1 = c0 + 1;
-      const uint32_t lo = c0 < T_mask ? __ldg(h + c0) : ninf;
-      const uint32_t hi = c1 < T_mask ? __ldg(h + c1) : ninf;
-      raw[v] = lo | (hi << 16);
+    for (int v = 0; v < 4; ++v) {
+      const int64_t e0 = (int64_t)c0 + 2 * v, e1 = e0 + 1;
+      const uint32_t lo = e0 < T_mask ? __ldg(h + e0) : ninf;
+      const uint32_t hi = e1 < T_mask ? __ldg(h + e1) : ninf;
+      w[v] = lo | (hi << 16);
     }
   }
+}
+
+// Additive-mask staging.  One warp copies the 128-column tile of its 32 mask rows into its
+// shared-memory region with coalesced cp.async (row-contiguous; 16-byte chunk c of row r at
+// r * 256 + (c ^ (r & 15)) * 16), so that each thread can then read its own row without bank
+// conflicts.  row0 is the warp's first mask row, row_bytes the row stride, rows the rows that
+// exist (the rest are not read), vec the alignment of every row start (4, 8 or 16 bytes).
+__device__ __forceinline__ void stage_mask_tile(uint32_t dst, const char* row0, int64_t row_bytes, int rows,
+                                                int vec, int lane) {
+  if (vec >= 16) {
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      const int r = 2 * n + (lane >> 4), c = lane & 15;
+      if (r < rows) ptx::cp_async16(dst + r * 256 + ((c ^ (r & 15)) << 4), row0 + r * row_bytes + c * 16);
+    }
+  } else if (vec >= 8) {
+#pragma unroll 8
+    for (int r = 0; r < 32; ++r)
+      if (r < rows)
+        ptx::cp_async8(dst + r * 256 + (((lane >> 1) ^ (r & 15)) << 4) + ((lane & 1) << 3), row0 + r * row_bytes + lane * 8);
+  } else {
+#pragma unroll 4
+    for (int r = 0; r < 32; ++r)
+      if (r < rows) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int q = h * 32 + lane;
+          ptx::cp_async4(dst + r * 256 + (((q >> 2) ^ (r & 15)) << 4) + ((q & 3) << 2), row0 + r * row_bytes + q * 4);
+        }
+      }
+  }
+  ptx::cp_async_commit();
 }
 
 template <typename M>
@@ -321,7 +354,8 @@ template <int H, bool kBF16, int kMode, int QT, int SPLIT, bool kStats>
 __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>::kMinBlocks)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const TcArgs a) {
-  using C = Cfg<H, QT>;
+  constexpr bool kStage = (kMode == kAddMask) && (SPLIT == 1);   // additive mask through shared memory
+  using C = Cfg<H, QT, kStage>;
   using Lay = Layout<QT, SPLIT>;
   constexpr int kQT = QT;
   constexpr int kSplit = SPLIT;                     // softmax threads per query row
@@ -584,6 +618,15 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
       mrow = reinterpret_cast<const char*>(a.r.add) +
              (b * a.r.add_sb + (int64_t)qh * a.r.add_sh + i * a.r.add_ss) * esz;
     }
+    // staged mask: the warp's first row, the row stride and how many of its 32 rows exist
+    const int64_t wrow = (int64_t)m0 + x * kBM + sub * 32;
+    const char* mwarp = nullptr;
+    int mrows = 0;
+    const uint32_t sMask = sbase + C::kMaskOff + (uint32_t)(x * 4 + sub) * C::kMaskWarpBytes;
+    if (kStage && a.add_stage) {
+      mwarp = reinterpret_cast<const char*>(a.r.add) + (b * a.r.add_sb + (int64_t)qh * a.r.add_sh + wrow * a.r.add_ss) * 2;
+      mrows = (int)max64(0, min64(32, (int64_t)a.S - wrow));
+    }
     const uint32_t trow = tmem + ((uint32_t)(sub * 32) << 16);
     const uint32_t tS = trow + (x == 0 ? C::kTmemS0 : C::kTmemS1) + kHalf * hh;
     const uint32_t tO = trow + (x == 0 ? C::kTmemO0 : C::kTmemO1) + (H / kSplit) * hh;
@@ -632,11 +675,12 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
 
     float m_use = (kMode == kCapFixed) ? m_fixed : -INFINITY, l = 0.f;
     for (int j = 0; j < n_tiles && ok; ++j) {
-      uint32_t mraw[kMode == kAddMask ? kHalf / 2 : 1];
-      if constexpr (kMode == kAddMask) {
-        // fetch this row's mask values for the tile now; the wait below hides the latency
-        if (valid)
-          prefetch_mask128(reinterpret_cast<const T*>(mrow), (kv_t0 + j) * kBN, a.r.add_T, a.add_vec, mraw);
+      bool staged = false;     // warp-uniform: the mask tile comes through shared memory
+      if constexpr (kStage) {
+        // copy the warp's mask rows for the tile now; the wait below hides the latency
+        const int k0 = (kv_t0 + j) * kBN;
+        staged = a.add_stage && (int64_t)k0 + kBN <= a.r.add_T;
+        if (staged) stage_mask_tile(sMask, mwarp + (int64_t)k0 * 2, a.r.add_ss * 2, mrows, a.add_vec, lane);
       }
       uint32_t kb[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};   // keep bits
       if constexpr (kMode == kKeep) {
@@ -658,6 +702,13 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
         // S_X(j) is in registers: the MMA warp may overwrite it with S_X(j+1)
         tc_fence_before();
         mbar_arrive(b_sfree(x));
+      }
+      if constexpr (kStage) {
+        if (staged) {
+          // the warp's copies have landed and are visible to every lane
+          ptx::cp_async_wait_all();
+          __syncwarp();
+        }
       }
 
       const int key0 = (kv_t0 + j) * kBN + kHalf * hh;
@@ -773,25 +824,43 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
         }
       } else if constexpr (kMode == kAddMask) {
         // additive mask / attention bias, then softcap (or the reverse), then the bounds;
-        // scores stay in natural units here (kfac carries log2 e)
-        if (!valid) {
+        // scores stay in natural units here (kfac carries log2 e).  The mask is read eight
+        // columns at a time: from the warp's staged rows, else from global memory.
+        static_assert(kSplit == 1, "the additive-mask mode covers 128 columns per thread");
+        auto run = [&](auto f) {
+          if (staged) {
+            const uint32_t rowp = sMask + lane * 256;
 #pragma unroll
-          for (int e = 0; e < kHalf; ++e) mraw[e >> 1] = 0u;
-        }
-        if (!a.has_softcap) {
+            for (int c = 0; c < kHalf / 8; ++c) {
+              uint32_t w[4];
+              ld_shared_v4(rowp + ((c ^ (lane & 15)) << 4), w[0], w[1], w[2], w[3]);
+              if (!valid) w[0] = w[1] = w[2] = w[3] = 0u;
 #pragma unroll
-          for (int e = 0; e < kHalf; ++e) s[e] = fmaf(s[e], a.scale, mask_elem<T>(mraw, e));
-        } else if (!a.r.softcap_before_bias) {
-          const float cin = 1.f / a.r.softcap;
+              for (int k = 0; k < 8; ++k) s[8 * c + k] = f(s[8 * c + k], mask_elem<T>(w, k));
+            }
+            __syncwarp();   // every lane has read its row: the region takes the next tile
+          } else {
 #pragma unroll
-          for (int e = 0; e < kHalf; ++e) {
-            const float v = fmaf(s[e], a.scale, mask_elem<T>(mraw, e));
-            s[e] = (v == -INFINITY) ? v : a.r.softcap * tanh_approx(v * cin);
+            for (int c = 0; c < kHalf / 8; ++c) {
+              uint32_t w[4] = {0u, 0u, 0u, 0u};
+              if (valid) load_mask_chunk(reinterpret_cast<const T*>(mrow), key0 + 8 * c, a.r.add_T, a.add_vec, w);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) s[8 * c + k] = f(s[8 * c + k], mask_elem<T>(w, k));
+            }
           }
+        };
+        if (!a.has_softcap) {
+          const float sc = a.scale;
+          run([sc](float sv, float mv) { return fmaf(sv, sc, mv); });
+        } else if (!a.r.softcap_before_bias) {
+          const float sc = a.scale, cap = a.r.softcap, cin = 1.f / a.r.softcap;
+          run([sc, cap, cin](float sv, float mv) {
+            const float v = fmaf(sv, sc, mv);
+            return (v == -INFINITY) ? v : cap * tanh_approx(v * cin);
+          });
         } else {
-#pragma unroll
-          for (int e = 0; e < kHalf; ++e)
-            s[e] = fmaf(a.r.softcap, tanh_approx(s[e] * a.cap_in), mask_elem<T>(mraw, e));
+          const float cap = a.r.softcap, cin = a.cap_in;
+          run([cap, cin](float sv, float mv) { return fmaf(cap, tanh_approx(sv * cin), mv); });
         }
         if (!((lo32 <= key0) && (key0 + kHalf - 1 <= hi32))) {
           const int elo = lo32 - key0, ehi = hi32 - key0;
@@ -908,6 +977,8 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
       tc_fence_before();
       mbar_arrive(b_pfull(x));
     }
+    // a loop left early may still have mask copies in flight into this warp's region
+    if constexpr (kStage) ptx::cp_async_wait_all();
 
     // ---- epilogue: O / (l + sink term), rounded once to the output type
     if (ok && n_tiles > 0) {
@@ -1045,7 +1116,7 @@ uint64_t wait_limit_ns() {
 template <int H, bool kBF16, int kMode, int QT, int SPLIT, bool kStats = false>
 cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, TcArgs a,
                         int64_t units_per_qt_row, cudaStream_t st) {
-  using C = Cfg<H, QT>;
+  using C = Cfg<H, QT, (kMode == kAddMask) && (SPLIT == 1)>;
   using Lay = Layout<QT, SPLIT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -1167,6 +1238,9 @@ cudaError_t launch_prefill_tc_stats(const Problem& p, sdpa_dtype dt, float* lse2
       if (st) g |= (uint64_t)(st * esz);
     a.add_vec = (int)(g & (~g + 1));   // lowest set bit
     if (a.add_vec > 16) a.add_vec = 16;
+    // rows aligned to 4 bytes or more: coalesced copies through shared memory (cp.async
+    // moves 4, 8 or 16 bytes); 2-byte-aligned rows keep the per-thread loads
+    a.add_stage = esz == 2 && a.add_vec >= 4;
   }
   a.cap_fixed = dt == SDPA_BF16 && a.has_softcap && p.r.softcap <= 40.f && !a.generic && !a.add_fast && !a.keep_fast;
   a.r = p.r;

@@ -133,6 +133,24 @@ def test_sweep_decode(case):
     run_and_compare(case, "decode")
 
 
+# ----------------------------------------------------------------- additive-mask row alignments
+
+# Mask rows of Tm 16-bit columns start 4-, 8- or 16-byte aligned (Tm = 258, 260, 264) or only
+# 2-byte aligned (Tm = 259); full mask tiles are staged through shared memory when the rows
+# allow 4-byte copies, and the ragged last tile and 2-byte rows are read per thread.  S = 150
+# leaves a partial query tile and partial 32-row groups.
+@pytest.mark.parametrize("Tm", [258, 259, 260, 264])
+@pytest.mark.parametrize("cap", ["none", "after", "before"])
+def test_additive_mask_row_alignments(Tm, cap):
+    for dtype, H in ((torch.float16, 64), (torch.bfloat16, 128)):
+        c = make_case(f"addmask_t{Tm}_{cap}", dtype=dtype, B=2, Nq=4, Nkv=2, S=150, L=300, H=H, seed=40 + Tm,
+                      add_mask="float", add_mask_shape=(2, 1, 150, Tm), add_mask_range=(-2.0, 1.0),
+                      softcap=0.0 if cap == "none" else 5.0, softcap_before_bias=cap == "before",
+                      causal="lower_right" if Tm % 2 else "none")
+        err, name = run_and_compare(c, "fwd")
+        assert name.startswith("prefill_tc"), name
+
+
 # ----------------------------------------------------------------- edge cases
 
 def test_no_keys_gives_zeros_and_sink_keeps_zero():
