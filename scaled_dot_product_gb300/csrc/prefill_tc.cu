@@ -436,29 +436,35 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
   // tiles run one step ahead: K_0, K_1, V_0, K_2, V_1, ...
   if (warp == 0) {
     // ================================================================ TMA producer
-    if (lane == 0 && n_tiles > 0) {
-      prefetch_tmap(&tq);
-      prefetch_tmap(&tk);
-      prefetch_tmap(&tv);
-      int c1, c2, c3;
-      mbar_arrive_expect_tx(b_q, kQT * C::kQTile);
-      for (int x = 0; x < kQT; ++x) {
-        perm_coords(a.q_ds, a.q_dn, a.q_db, m0 + x * kBM, qh, b, c1, c2, c3);
-        for (int r = 0; r < C::kRegions; ++r)
-          tma_load_4d(sQ + x * C::kQTile + r * C::kRegionBytes, &tq, b_q, 64 * r, c1, c2, c3);
+    // (the whole warp runs the loop and one elected lane issues the copies)
+    if (n_tiles > 0) {
+      const uint32_t leader = elect_one();
+      if (leader) {
+        prefetch_tmap(&tq);
+        prefetch_tmap(&tk);
+        prefetch_tmap(&tv);
+        int c1, c2, c3;
+        mbar_arrive_expect_tx(b_q, kQT * C::kQTile);
+        for (int x = 0; x < kQT; ++x) {
+          perm_coords(a.q_ds, a.q_dn, a.q_db, m0 + x * kBM, qh, b, c1, c2, c3);
+          for (int r = 0; r < C::kRegions; ++r)
+            tma_load_4d(sQ + x * C::kQTile + r * C::kRegionBytes, &tq, b_q, 64 * r, c1, c2, c3);
+        }
       }
       int seq = 0;
       bool ok = true;
       auto load = [&](const CUtensorMap* map, int tile) -> bool {
         const int st = seq % C::kStages;
         if (seq >= C::kStages &&
-            !mbar_wait_bounded(b_empty(st), ((seq / C::kStages) - 1) & 1, abortp, a.wait_ns))
+            !__all_sync(0xffffffffu, mbar_wait_bounded(b_empty(st), ((seq / C::kStages) - 1) & 1, abortp, a.wait_ns)))
           return false;
-        mbar_arrive_expect_tx(b_full(st), C::kKVTile);
-        int d1, d2, d3;
-        perm_coords(a.kv_ds, a.kv_dn, a.kv_db, (kv_t0 + tile) * kBN, kvh, b, d1, d2, d3);
-        for (int r = 0; r < C::kRegions; ++r)
-          tma_load_4d(sKV + st * C::kKVTile + r * C::kRegionBytes, map, b_full(st), 64 * r, d1, d2, d3);
+        if (leader) {
+          mbar_arrive_expect_tx(b_full(st), C::kKVTile);
+          int d1, d2, d3;
+          perm_coords(a.kv_ds, a.kv_dn, a.kv_db, (kv_t0 + tile) * kBN, kvh, b, d1, d2, d3);
+          for (int r = 0; r < C::kRegions; ++r)
+            tma_load_4d(sKV + st * C::kKVTile + r * C::kRegionBytes, map, b_full(st), 64 * r, d1, d2, d3);
+        }
         ++seq;
         return true;
       };
@@ -472,7 +478,7 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
           if (ok) ok = load(&tv, j);
         }
       }
-      if (!ok || *abortp) {
+      if (__any_sync(0xffffffffu, !ok || *abortp)) {
         // some role gave up: let every copy already issued land before the CTA can exit
         mbar_wait_bounded(b_q, 0, nullptr, kDrainNs);
         for (int s = 0; s < C::kStages && s < seq; ++s) {
@@ -484,7 +490,16 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    if (lane == 0 && n_tiles > 0) {
+    // (the whole warp runs the loop; one elected lane issues every MMA and every commit, as a
+    // commit tracks the MMAs of the thread that issues it)
+    if (n_tiles > 0) {
+      const uint32_t leader = elect_one();
+      auto commit = [&](uint32_t bar) {
+        if (leader) mma_commit(bar);
+      };
+      auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+        return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abortp, a.wait_ns));
+      };
       constexpr uint32_t kIdQK = idesc_f16(kBF16, kBM, kBN, false);
       constexpr uint32_t kIdPV = idesc_f16(kBF16, kBM, H, true);
       const uint32_t tS[2] = {tmem + C::kTmemS0, tmem + C::kTmemS1};   // [1] unused with one tile
@@ -492,7 +507,7 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
       const uint32_t tP[2] = {tmem + C::kTmemP0, tmem + C::kTmemP1};
       int seq = 0;
       auto wait_full = [&](int sq) -> bool {
-        const bool ok = mbar_wait_bounded(b_full(sq % C::kStages), (sq / C::kStages) & 1, abortp, a.wait_ns);
+        const bool ok = wait_all(b_full(sq % C::kStages), (sq / C::kStages) & 1);
         tc_fence_after();
         return ok;
       };
@@ -505,25 +520,25 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
 #pragma unroll
         for (int kk = 0; kk < H / 16; ++kk) {
           const uint64_t off = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
-          mma_f16_ss(tS[x], dQ[x] + off, dk + off, kIdQK, kk > 0);
+          if (leader) mma_f16_ss(tS[x], dQ[x] + off, dk + off, kIdQK, kk > 0);
         }
       };
       auto issue_PV = [&](int x, int st, bool acc) {
         const uint64_t dv = dV0 + (uint64_t)((st * C::kKVTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_f16_ts(tO[x], tP[x] + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdPV, (acc || kk > 0) ? 1u : 0u);
+          if (leader) mma_f16_ts(tO[x], tP[x] + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdPV, (acc || kk > 0) ? 1u : 0u);
       };
-      bool ok = mbar_wait_bounded(a.q_bias ? b_qready : b_q, 0, abortp, a.wait_ns);
+      bool ok = wait_all(a.q_bias ? b_qready : b_q, 0);
       tc_fence_after();
       if (ok) ok = wait_full(seq);
       if (ok) {
         const int st = seq % C::kStages;
         for (int x = 0; x < kQT; ++x) {
           issue_S(x, st);
-          mma_commit(b_sfull(x));
+          commit(b_sfull(x));
         }
-        mma_commit(b_empty(st));
+        commit(b_empty(st));
         ++seq;
       }
       if constexpr (C::kAlias) {
@@ -536,19 +551,19 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
           ++seq;
           const int kst = seq % C::kStages;
           for (int x = 0; x < kQT && ok; ++x) {
-            if (!(ok = mbar_wait_bounded(b_pfull(x), j & 1, abortp, a.wait_ns))) break;
+            if (!(ok = wait_all(b_pfull(x), j & 1))) break;
             tc_fence_after();
             issue_PV(x, vst, j > 0);
             if (more) {
               if (x == 0 && !(ok = wait_full(seq))) break;
               issue_S(x, kst);
             }
-            mma_commit(b_sfull(x));
+            commit(b_sfull(x));
           }
           if (!ok) break;
-          mma_commit(b_empty(vst));
+          commit(b_empty(vst));
           if (more) {
-            mma_commit(b_empty(kst));
+            commit(b_empty(kst));
             ++seq;
           }
         }
@@ -560,29 +575,29 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
             if (!(ok = wait_full(seq))) break;
             ++seq;
             for (int x = 0; x < kQT && ok; ++x) {
-              if (!(ok = mbar_wait_bounded(b_sfree(x), j & 1, abortp, a.wait_ns))) break;
+              if (!(ok = wait_all(b_sfree(x), j & 1))) break;
               tc_fence_after();
               issue_S(x, kst);
-              mma_commit(b_sfull(x));
+              commit(b_sfull(x));
             }
             if (!ok) break;
-            mma_commit(b_empty(kst));
+            commit(b_empty(kst));
           }
           const int vst = seq % C::kStages;
           if (!(ok = wait_full(seq))) break;
           ++seq;
           for (int x = 0; x < kQT && ok; ++x) {
-            if (!(ok = mbar_wait_bounded(b_pfull(x), j & 1, abortp, a.wait_ns))) break;
+            if (!(ok = wait_all(b_pfull(x), j & 1))) break;
             tc_fence_after();
             issue_PV(x, vst, j > 0);
-            mma_commit(b_odone(x));
+            commit(b_odone(x));
           }
           if (!ok) break;
-          mma_commit(b_empty(vst));
+          commit(b_empty(vst));
         }
       }
       // every MMA this thread issued completes before the CTA frees its tensor memory
-      mma_commit(b_drain);
+      commit(b_drain);
       mbar_wait_bounded(b_drain, 0, nullptr, kDrainNs);
     }
     __syncwarp();
