@@ -334,30 +334,33 @@ __global__ void __launch_bounds__(BCfg<H, STEP>::kThreads, BCfg<H, STEP>::kMinBl
 
   if (warp == 0) {
     // ======================================================== TMA producer
-    if (lane == 0 && n_steps > 0) {
-      prefetch_tmap(&tq); prefetch_tmap(&tg); prefetch_tmap(&tk); prefetch_tmap(&tv);
+    if (n_steps > 0) {
+      const uint32_t leader = elect_one();   // issues every copy, MMA and commit of the warp
+      if (leader) {
+        prefetch_tmap(&tq); prefetch_tmap(&tg); prefetch_tmap(&tk); prefetch_tmap(&tv);
+      }
       int c1, c2, c3;
-      mbar_arrive_expect_tx(b_kv, 2 * C::kTile);
+      if (leader) mbar_arrive_expect_tx(b_kv, 2 * C::kTile);
       perm_coords(a.kv_ds, a.kv_dn, a.kv_db, (int)k0, kvh, b, c1, c2, c3);
       for (int r = 0; r < C::kRegions; ++r) {
-        tma_load_4d(sK + r * C::kRegionBytes, &tk, b_kv, 64 * r, c1, c2, c3);
-        tma_load_4d(sV + r * C::kRegionBytes, &tv, b_kv, 64 * r, c1, c2, c3);
+        if (leader) tma_load_4d(sK + r * C::kRegionBytes, &tk, b_kv, 64 * r, c1, c2, c3);
+        if (leader) tma_load_4d(sV + r * C::kRegionBytes, &tv, b_kv, 64 * r, c1, c2, c3);
       }
       int n = 0;
       for (; n < n_steps; ++n) {
         const int st = n % C::kStages;
         if (n >= C::kStages &&
-            !mbar_wait_bounded(b_empty(st), ((n / C::kStages) - 1) & 1, abortp, a.wait_ns))
+            !__all_sync(0xffffffffu, mbar_wait_bounded(b_empty(st), ((n / C::kStages) - 1) & 1, abortp, a.wait_ns)))
           break;
         const int qt = qt_lo + n / a.group, h = kvh * a.group + n % a.group;
         const uint32_t sQ = sRing + st * 2 * C::kSTile, sG = sQ + C::kSTile;
-        mbar_arrive_expect_tx(b_full(st), 2 * C::kSTile);
+        if (leader) mbar_arrive_expect_tx(b_full(st), 2 * C::kSTile);
         perm_coords(a.q_ds, a.q_dn, a.q_db, qt * STEP, h, b, c1, c2, c3);
-        for (int r = 0; r < C::kRegions; ++r) tma_load_4d(sQ + r * C::kSRegionBytes, &tq, b_full(st), 64 * r, c1, c2, c3);
+        for (int r = 0; r < C::kRegions; ++r) if (leader) tma_load_4d(sQ + r * C::kSRegionBytes, &tq, b_full(st), 64 * r, c1, c2, c3);
         perm_coords(a.g_ds, a.g_dn, a.g_db, qt * STEP, h, b, c1, c2, c3);
-        for (int r = 0; r < C::kRegions; ++r) tma_load_4d(sG + r * C::kSRegionBytes, &tg, b_full(st), 64 * r, c1, c2, c3);
+        for (int r = 0; r < C::kRegions; ++r) if (leader) tma_load_4d(sG + r * C::kSRegionBytes, &tg, b_full(st), 64 * r, c1, c2, c3);
       }
-      if (n < n_steps || *abortp) {
+      if (__any_sync(0xffffffffu, n < n_steps || *abortp)) {
         // some role gave up: let every copy already issued land before the CTA can exit
         mbar_wait_bounded(b_kv, 0, nullptr, kDrainNs);
         for (int s = 0; s < C::kStages && s < n; ++s) {
@@ -369,17 +372,18 @@ __global__ void __launch_bounds__(BCfg<H, STEP>::kThreads, BCfg<H, STEP>::kMinBl
     __syncwarp();
   } else if (warp == 1) {
     // ======================================================== MMA issuer
-    if (lane == 0 && n_steps > 0) {
+    if (n_steps > 0) {
+      const uint32_t leader = elect_one();   // issues every copy, MMA and commit of the warp
       constexpr uint32_t kIdS = idesc_f16(kBF16, kBM, STEP, false);  // M keys, N queries
       constexpr uint32_t kIdA = idesc_f16(kBF16, kBM, H, true);      // M keys, N head dims
       const uint32_t tS = tmem + C::kTmemS, tP = tmem + C::kTmemP;
       const uint32_t tdK = tmem + C::kTmemA0, tdV = tmem + C::kTmemA1;
       const uint64_t dK = desc_sw128(sK, 16, 1024), dV = desc_sw128(sV, 16, 1024);
-      bool ok = mbar_wait_bounded(b_kv, 0, abortp, a.wait_ns);
+      bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_kv, 0, abortp, a.wait_ns));
       tc_fence_after();
       for (int n = 0; n < n_steps && ok; ++n) {
         const int st = n % C::kStages;
-        if (!(ok = mbar_wait_bounded(b_full(st), (n / C::kStages) & 1, abortp, a.wait_ns))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_full(st), (n / C::kStages) & 1, abortp, a.wait_ns)))) break;
         tc_fence_after();
         const uint32_t sQ = sRing + st * 2 * C::kSTile, sG = sQ + C::kSTile;
         const uint64_t dQk = desc_sw128(sQ, 16, 1024), dGk = desc_sw128(sG, 16, 1024);
@@ -389,28 +393,28 @@ __global__ void __launch_bounds__(BCfg<H, STEP>::kThreads, BCfg<H, STEP>::kMinBl
         for (int kk = 0; kk < H / 16; ++kk) {
           const uint64_t offa = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
           const uint64_t offb = (uint64_t)(((kk / 4) * C::kSRegionBytes + (kk % 4) * 32) >> 4);
-          mma_f16_ss(tS, dK + offa, dQk + offb, kIdS, kk > 0);
+          if (leader) mma_f16_ss(tS, dK + offa, dQk + offb, kIdS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < H / 16; ++kk) {
           const uint64_t offa = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
           const uint64_t offb = (uint64_t)(((kk / 4) * C::kSRegionBytes + (kk % 4) * 32) >> 4);
-          mma_f16_ss(tP, dV + offa, dGk + offb, kIdS, kk > 0);
+          if (leader) mma_f16_ss(tP, dV + offa, dGk + offb, kIdS, kk > 0);
         }
-        mma_commit(b_sready);
-        if (!(ok = mbar_wait_bounded(b_pready, n & 1, abortp, a.wait_ns))) break;
+        if (leader) mma_commit(b_sready);
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_pready, n & 1, abortp, a.wait_ns)))) break;
         tc_fence_after();
         // dV += P^T dY and dK += dS^T Q: A from TMEM (16 queries = 8 columns per K step)
 #pragma unroll
         for (int kk = 0; kk < STEP / 16; ++kk)
-          mma_f16_ts(tdV, tS + kk * 8, dGm + (uint64_t)((kk * 2048) >> 4), kIdA, (n > 0 || kk > 0) ? 1u : 0u);
+          if (leader) mma_f16_ts(tdV, tS + kk * 8, dGm + (uint64_t)((kk * 2048) >> 4), kIdA, (n > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < STEP / 16; ++kk)
-          mma_f16_ts(tdK, tP + kk * 8, dQm + (uint64_t)((kk * 2048) >> 4), kIdA, (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(b_empty(st));
+          if (leader) mma_f16_ts(tdK, tP + kk * 8, dQm + (uint64_t)((kk * 2048) >> 4), kIdA, (n > 0 || kk > 0) ? 1u : 0u);
+        if (leader) mma_commit(b_empty(st));
       }
       // the accumulators are final (or the CTA gave up) once every MMA completes
-      mma_commit(b_acc);
+      if (leader) mma_commit(b_acc);
       mbar_wait_bounded(b_acc, 0, nullptr, kDrainNs);
     }
     __syncwarp();
@@ -538,29 +542,32 @@ __global__ void __launch_bounds__(BCfg<H, STEP>::kThreads, BCfg<H, STEP>::kMinBl
 
   if (warp == 0) {
     // ======================================================== TMA producer
-    if (lane == 0 && n_steps > 0) {
-      prefetch_tmap(&tq); prefetch_tmap(&tg); prefetch_tmap(&tk); prefetch_tmap(&tv);
+    if (n_steps > 0) {
+      const uint32_t leader = elect_one();   // issues every copy, MMA and commit of the warp
+      if (leader) {
+        prefetch_tmap(&tq); prefetch_tmap(&tg); prefetch_tmap(&tk); prefetch_tmap(&tv);
+      }
       int c1, c2, c3;
-      mbar_arrive_expect_tx(b_q, 2 * C::kTile);
+      if (leader) mbar_arrive_expect_tx(b_q, 2 * C::kTile);
       perm_coords(a.q_ds, a.q_dn, a.q_db, (int)m0, qh, b, c1, c2, c3);
-      for (int r = 0; r < C::kRegions; ++r) tma_load_4d(sQ + r * C::kRegionBytes, &tq, b_q, 64 * r, c1, c2, c3);
+      for (int r = 0; r < C::kRegions; ++r) if (leader) tma_load_4d(sQ + r * C::kRegionBytes, &tq, b_q, 64 * r, c1, c2, c3);
       perm_coords(a.g_ds, a.g_dn, a.g_db, (int)m0, qh, b, c1, c2, c3);
-      for (int r = 0; r < C::kRegions; ++r) tma_load_4d(sG + r * C::kRegionBytes, &tg, b_q, 64 * r, c1, c2, c3);
+      for (int r = 0; r < C::kRegions; ++r) if (leader) tma_load_4d(sG + r * C::kRegionBytes, &tg, b_q, 64 * r, c1, c2, c3);
       int n = 0;
       for (; n < n_steps; ++n) {
         const int st = n % C::kStages;
         if (n >= C::kStages &&
-            !mbar_wait_bounded(b_empty(st), ((n / C::kStages) - 1) & 1, abortp, a.wait_ns))
+            !__all_sync(0xffffffffu, mbar_wait_bounded(b_empty(st), ((n / C::kStages) - 1) & 1, abortp, a.wait_ns)))
           break;
         const uint32_t sK = sRing + st * 2 * C::kSTile, sV = sK + C::kSTile;
-        mbar_arrive_expect_tx(b_full(st), 2 * C::kSTile);
+        if (leader) mbar_arrive_expect_tx(b_full(st), 2 * C::kSTile);
         perm_coords(a.kv_ds, a.kv_dn, a.kv_db, (kt0 + n) * STEP, kvh, b, c1, c2, c3);
         for (int r = 0; r < C::kRegions; ++r) {
-          tma_load_4d(sK + r * C::kSRegionBytes, &tk, b_full(st), 64 * r, c1, c2, c3);
-          tma_load_4d(sV + r * C::kSRegionBytes, &tv, b_full(st), 64 * r, c1, c2, c3);
+          if (leader) tma_load_4d(sK + r * C::kSRegionBytes, &tk, b_full(st), 64 * r, c1, c2, c3);
+          if (leader) tma_load_4d(sV + r * C::kSRegionBytes, &tv, b_full(st), 64 * r, c1, c2, c3);
         }
       }
-      if (n < n_steps || *abortp) {
+      if (__any_sync(0xffffffffu, n < n_steps || *abortp)) {
         mbar_wait_bounded(b_q, 0, nullptr, kDrainNs);
         for (int s = 0; s < C::kStages && s < n; ++s) {
           const int last = s + ((n - 1 - s) / C::kStages) * C::kStages;
@@ -571,16 +578,17 @@ __global__ void __launch_bounds__(BCfg<H, STEP>::kThreads, BCfg<H, STEP>::kMinBl
     __syncwarp();
   } else if (warp == 1) {
     // ======================================================== MMA issuer
-    if (lane == 0 && n_steps > 0) {
+    if (n_steps > 0) {
+      const uint32_t leader = elect_one();   // issues every copy, MMA and commit of the warp
       constexpr uint32_t kIdS = idesc_f16(kBF16, kBM, STEP, false);  // M queries, N keys
       constexpr uint32_t kIdA = idesc_f16(kBF16, kBM, H, true);      // M queries, N head dims
       const uint32_t tS = tmem + C::kTmemS, tP = tmem + C::kTmemP, tdQ = tmem + C::kTmemA0;
       const uint64_t dQ = desc_sw128(sQ, 16, 1024), dG = desc_sw128(sG, 16, 1024);
-      bool ok = mbar_wait_bounded(b_q, 0, abortp, a.wait_ns);
+      bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_q, 0, abortp, a.wait_ns));
       tc_fence_after();
       for (int n = 0; n < n_steps && ok; ++n) {
         const int st = n % C::kStages;
-        if (!(ok = mbar_wait_bounded(b_full(st), (n / C::kStages) & 1, abortp, a.wait_ns))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_full(st), (n / C::kStages) & 1, abortp, a.wait_ns)))) break;
         tc_fence_after();
         const uint32_t sK = sRing + st * 2 * C::kSTile, sV = sK + C::kSTile;
         const uint64_t dKk = desc_sw128(sK, 16, 1024), dVk = desc_sw128(sV, 16, 1024);
@@ -590,24 +598,24 @@ __global__ void __launch_bounds__(BCfg<H, STEP>::kThreads, BCfg<H, STEP>::kMinBl
         for (int kk = 0; kk < H / 16; ++kk) {
           const uint64_t offa = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
           const uint64_t offb = (uint64_t)(((kk / 4) * C::kSRegionBytes + (kk % 4) * 32) >> 4);
-          mma_f16_ss(tS, dQ + offa, dKk + offb, kIdS, kk > 0);
+          if (leader) mma_f16_ss(tS, dQ + offa, dKk + offb, kIdS, kk > 0);
         }
 #pragma unroll
         for (int kk = 0; kk < H / 16; ++kk) {
           const uint64_t offa = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
           const uint64_t offb = (uint64_t)(((kk / 4) * C::kSRegionBytes + (kk % 4) * 32) >> 4);
-          mma_f16_ss(tP, dG + offa, dVk + offb, kIdS, kk > 0);
+          if (leader) mma_f16_ss(tP, dG + offa, dVk + offb, kIdS, kk > 0);
         }
-        mma_commit(b_sready);
-        if (!(ok = mbar_wait_bounded(b_pready, n & 1, abortp, a.wait_ns))) break;
+        if (leader) mma_commit(b_sready);
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_pready, n & 1, abortp, a.wait_ns)))) break;
         tc_fence_after();
         // dQ += dS K: dS from TMEM (16 keys = 8 columns per K step), K MN-major
 #pragma unroll
         for (int kk = 0; kk < STEP / 16; ++kk)
-          mma_f16_ts(tdQ, tS + kk * 8, dKm + (uint64_t)((kk * 2048) >> 4), kIdA, (n > 0 || kk > 0) ? 1u : 0u);
-        mma_commit(b_empty(st));
+          if (leader) mma_f16_ts(tdQ, tS + kk * 8, dKm + (uint64_t)((kk * 2048) >> 4), kIdA, (n > 0 || kk > 0) ? 1u : 0u);
+        if (leader) mma_commit(b_empty(st));
       }
-      mma_commit(b_acc);
+      if (leader) mma_commit(b_acc);
       mbar_wait_bounded(b_acc, 0, nullptr, kDrainNs);
     }
     __syncwarp();

@@ -160,27 +160,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ================================================================ TMA producer
-    if (lane == 0 && nit > 0) {
-      prefetch_tmap(&tq);
-      prefetch_tmap(&tk);
+    if (nit > 0) {
+      const uint32_t leader = elect_one();   // issues every copy, MMA and commit of the warp
+      if (leader) prefetch_tmap(&tq);
+      if (leader) prefetch_tmap(&tk);
       int c1, c2, c3;
-      mbar_arrive_expect_tx(b_q, C::kTile);
+      if (leader) mbar_arrive_expect_tx(b_q, C::kTile);
       perm3(a.q_ds, a.q_dn, a.q_db, m0, h, b, c1, c2, c3);
-      for (int r = 0; r < C::kRegions; ++r) tma_load_4d(sQ + r * C::kRegionBytes, &tq, b_q, 64 * r, c1, c2, c3);
+      for (int r = 0; r < C::kRegions; ++r) if (leader) tma_load_4d(sQ + r * C::kRegionBytes, &tq, b_q, 64 * r, c1, c2, c3);
       int issued = 0;
       bool ok = true;
       for (int it = 0; it < nit && ok; ++it) {
         const int st = it % C::kStages;
         if (it >= C::kStages &&
-            !(ok = mbar_wait_bounded(b_empty(st), ((it / C::kStages) - 1) & 1, abortp, a.wait_ns)))
+            !(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_empty(st), ((it / C::kStages) - 1) & 1, abortp, a.wait_ns))))
           break;
-        mbar_arrive_expect_tx(b_full(st), C::kTile);
+        if (leader) mbar_arrive_expect_tx(b_full(st), C::kTile);
         perm3(a.k_ds, a.k_dn, a.k_db, (it % nT) * kKeys, kvh, b, c1, c2, c3);
         for (int r = 0; r < C::kRegions; ++r)
-          tma_load_4d(sK + st * C::kTile + r * C::kRegionBytes, &tk, b_full(st), 64 * r, c1, c2, c3);
+          if (leader) tma_load_4d(sK + st * C::kTile + r * C::kRegionBytes, &tk, b_full(st), 64 * r, c1, c2, c3);
         ++issued;
       }
-      if (!ok || *abortp) {
+      if (__any_sync(0xffffffffu, !ok || *abortp)) {
         // some role gave up: let every copy already issued land before the CTA can exit
         mbar_wait_bounded(b_q, 0, nullptr, kDrainNs);
         for (int s = 0; s < C::kStages && s < issued; ++s) {
@@ -192,31 +193,32 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
-    if (lane == 0 && nit > 0) {
+    if (nit > 0) {
+      const uint32_t leader = elect_one();   // issues every copy, MMA and commit of the warp
       constexpr uint32_t kId = idesc_f16(kBF16, kRows, kKeys, false);
       const uint64_t dQ = desc_sw128(sQ, 16, 1024);
       const uint64_t dK0 = desc_sw128(sK, 16, 1024);
-      bool ok = mbar_wait_bounded(b_q, 0, abortp, a.wait_ns);
+      bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_q, 0, abortp, a.wait_ns));
       tc_fence_after();
       for (int it = 0; it < nit && ok; ++it) {
         const int buf = it & 1, st = it % C::kStages;
         if (it >= 2) {
-          if (!(ok = mbar_wait_bounded(b_sfree(buf), ((it >> 1) - 1) & 1, abortp, a.wait_ns))) break;
+          if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_sfree(buf), ((it >> 1) - 1) & 1, abortp, a.wait_ns)))) break;
           tc_fence_after();
         }
-        if (!(ok = mbar_wait_bounded(b_full(st), (it / C::kStages) & 1, abortp, a.wait_ns))) break;
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_full(st), (it / C::kStages) & 1, abortp, a.wait_ns)))) break;
         tc_fence_after();
         const uint64_t dk = dK0 + (uint64_t)((st * C::kTile) >> 4);
 #pragma unroll
         for (int kk = 0; kk < H / 16; ++kk) {
           const uint64_t off = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
-          mma_f16_ss(tmem + buf * kKeys, dQ + off, dk + off, kId, kk > 0);
+          if (leader) mma_f16_ss(tmem + buf * kKeys, dQ + off, dk + off, kId, kk > 0);
         }
-        mma_commit(b_sfull(buf));
-        mma_commit(b_empty(st));
+        if (leader) mma_commit(b_sfull(buf));
+        if (leader) mma_commit(b_empty(st));
       }
       // every MMA this thread issued completes before the CTA frees its tensor memory
-      mma_commit(b_drain);
+      if (leader) mma_commit(b_drain);
       mbar_wait_bounded(b_drain, 0, nullptr, kDrainNs);
     }
     __syncwarp();

@@ -63,14 +63,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking test of the same phase.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok;
+}
+
 // Waits for phase `parity` of barrier `bar`.  Gives up when *abort becomes non-zero or
-// after limit_ns nanoseconds (then sets *abort); returns false in both cases.
+// after limit_ns nanoseconds (then sets *abort); returns false in both cases.  Limits below
+// a microsecond (a test setting) poll without suspending, so that every wait that is not
+// already satisfied runs out: try_wait may suspend the thread for longer than the limit.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                                   uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  const bool poll = limit_ns < 1000;
+  if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (abort && *abort) return false;
     if (globaltimer() - t0 > limit_ns) {
       if (abort) *abort = 1;
