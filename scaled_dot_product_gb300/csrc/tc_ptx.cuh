@@ -78,12 +78,13 @@ __device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for phase `parity` of barrier `bar`.  Gives up when *abort becomes non-zero or
 // after limit_ns nanoseconds (then sets *abort); returns false in both cases.  Limits below
-// a microsecond (a test setting) poll without suspending, so that every wait that is not
-// already satisfied runs out: try_wait may suspend the thread for longer than the limit.
+// a microsecond are a test setting: the wait then polls without suspending, so that every
+// wait that is not already satisfied runs out (a try_wait may suspend its thread for longer
+// than such a limit and succeed).  The common path stays one test and one try_wait.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort,
                                                   uint64_t limit_ns) {
   const bool poll = limit_ns < 1000;
-  if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  if (!poll && mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer();
   for (;;) {
     if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
