@@ -177,9 +177,9 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
       : "memory");
 }
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far completes.
-// One lane of a converged warp (the same lane on every call with all lanes active); the
-// issue loops of the producer and MMA warps run on the whole warp and let this lane issue,
-// which keeps their addresses and descriptors warp-uniform.
+// One lane of a converged warp.  The issue loops of the producer and MMA warps run on the
+// whole warp, compute this once and let that lane issue every copy, MMA and commit, which
+// keeps their addresses and descriptors warp-uniform.
 __device__ __forceinline__ uint32_t elect_one() {
   uint32_t pred = 0;
   asm volatile(
