@@ -19,6 +19,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -160,14 +161,30 @@ KERNEL_SOURCES = {
 }
 
 
-def source_digest(kernel: str) -> str:
+_CODE_TOKENS = re.compile(r'"(?:\\.|[^"\\\n])*"|\'(?:\\.|[^\'\\\n])*\'|//[^\n]*|/\*.*?\*/', re.S)
+
+
+def strip_comments(src: str) -> str:
+    """C/C++/CUDA source without its comments (string and character literals kept), with
+    trailing blanks and blank lines dropped: what the compiler sees, for the digest."""
+    code = _CODE_TOKENS.sub(lambda m: m.group(0) if m.group(0)[0] in "\"'" else " ", src)
+    lines = (ln.rstrip() for ln in code.splitlines())
+    return "\n".join(ln for ln in lines if ln)
+
+
+def source_digest(kernel: str, read=None) -> str:
+    """Digest of the kernel family's sources without comments: counters taken on the sources
+    stay valid through comment edits and are dropped on any code change.  `read(name)` returns
+    a source's text (default: the working tree)."""
     fam = next((f for f in KERNEL_SOURCES if kernel.startswith(f)), None)
     csrc = os.path.join(ROOT, "scaled_dot_product_gb300", "csrc")
     names = KERNEL_SOURCES[fam] if fam else tuple(sorted(os.listdir(csrc)))
+    if read is None:
+        read = lambda n: open(os.path.join(csrc, n), encoding="utf-8").read()
     h = hashlib.sha256()
     for n in names:
         h.update(n.encode())
-        h.update(open(os.path.join(csrc, n), "rb").read())
+        h.update(strip_comments(read(n)).encode())
     return h.hexdigest()[:16]
 
 
