@@ -170,48 +170,6 @@ __device__ __forceinline__ void key_bounds(const TcArgs& a, int64_t len_b, int64
   if (a.len_kind == SDPA_LEN_SEQLENS_K_I32) hi = min64(hi, len_b);
 }
 
-// Mask values of keys [k0, k0 + 32) of one row, as floats; keys >= T_mask read -inf.
-template <typename M>
-__device__ __forceinline__ void load_mask32_t(const M* row, int k0, int64_t T_mask, int vec_bytes, float* out) {
-  if ((int64_t)k0 + 32 <= T_mask) {
-    const M* p = row + k0;
-    if (vec_bytes >= 16) {
-      constexpr int per = 16 / sizeof(M);
-#pragma unroll
-      for (int v = 0; v < 32 / per; ++v) {
-        const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + v);
-        const M* e = reinterpret_cast<const M*>(&u);
-#pragma unroll
-        for (int x = 0; x < per; ++x) out[v * per + x] = Elem<M>::to_f32(e[x]);
-      }
-    } else if (vec_bytes >= 8) {
-      constexpr int per = 8 / sizeof(M);
-#pragma unroll
-      for (int v = 0; v < 32 / per; ++v) {
-        const uint2 u = __ldg(reinterpret_cast<const uint2*>(p) + v);
-        const M* e = reinterpret_cast<const M*>(&u);
-#pragma unroll
-        for (int x = 0; x < per; ++x) out[v * per + x] = Elem<M>::to_f32(e[x]);
-      }
-    } else {
-#pragma unroll
-      for (int x = 0; x < 32; ++x) out[x] = Elem<M>::to_f32(p[x]);
-    }
-  } else {
-#pragma unroll
-    for (int x = 0; x < 32; ++x) out[x] = ((int64_t)k0 + x < T_mask) ? Elem<M>::to_f32(row[k0 + x]) : -INFINITY;
-  }
-}
-
-__device__ __forceinline__ void load_mask32(const void* row, int dtype, int k0, int64_t T_mask, int vec_bytes,
-                                            float* out) {
-  if (dtype == SDPA_F16) load_mask32_t(reinterpret_cast<const __half*>(row), k0, T_mask, vec_bytes, out);
-  else if (dtype == SDPA_BF16) load_mask32_t(reinterpret_cast<const __nv_bfloat16*>(row), k0, T_mask, vec_bytes, out);
-  else load_mask32_t(reinterpret_cast<const float*>(row), k0, T_mask, vec_bytes, out);
-}
-
-// Mask values of keys [k0, k0 + 128) of one row, as 64 packed 16-bit pairs in the mask's
-// own type (element 2c in the low half of word c).  Keys >= T_mask read -inf.
 // Mask values of columns c0 .. c0+7 of one 16-bit mask row into w[4] (elements 2v, 2v+1 in
 // w[v]): the widest loads the row alignment vec allows, -inf past the mask's T_mask columns.
 template <typename M>
