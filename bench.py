@@ -201,7 +201,15 @@ def ncu_traffic(kernel: str):
 
 # ------------------------------------------------------------------------------ native arm
 
+HOST_LEAD_CYCLES = 4_000_000       # ~2 ms of GPU sleep ahead of the timed steps
+
+
 def time_device(fn, steps, warmup, flush_buf, barrier):
+    """CUDA-event times of `steps` calls of fn on the current stream (L2 flushed before each
+    when flush_buf is given, outside the events).  A short device-side sleep is queued ahead
+    of the first timed step, so that the host has enqueued the first steps before the GPU
+    reaches them: an event pair then brackets device work only, never the GPU idling while
+    the host prepares a call."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -210,6 +218,7 @@ def time_device(fn, steps, warmup, flush_buf, barrier):
     barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
+    torch.cuda._sleep(HOST_LEAD_CYCLES)
     for s in range(steps):
         if flush_buf is not None:
             flush_buf.fill_(s & 0xff)       # evict the inputs from L2 between timed steps

@@ -78,22 +78,26 @@ __device__ __forceinline__ float tanh_poly(float u) {
 
 template <int H, int kQT, bool kMaskStage = false>
 struct Cfg {
+  static_assert(kQT == 2, "two query tiles per CTA");
   static constexpr int kRegions = H / 64;              // 128-byte swizzle regions per row
   static constexpr int kRegionBytes = 128 * 128;       // 128 rows x 128 bytes
   static constexpr int kQTile = kBM * H * 2;
   static constexpr int kKVTile = kBN * H * 2;
-  // ring depth: fill the shared memory one CTA (two tiles) or half of it (one tile) may use;
-  // a staged additive mask takes 8 KB per softmax warp out of it
-  static constexpr int kStages = kMaskStage ? ((H == 128) ? 3 : 7)
-                                            : ((kQT == 2) ? ((H == 128) ? 4 : 10) : ((H == 128) ? 2 : 5));
+  // Q is double-buffered (the next unit's tiles load during the current unit); a finished
+  // unit's buffer then stages its output y for the TMA stores
+  static constexpr int kQBuf = kQT * kQTile;
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = kQT * kQTile;
+  static constexpr int kKVOff = 2 * kQBuf;
+  // K/V ring depth: what is left of the shared memory; a staged additive mask (H = 64 only)
+  // takes 8 KB per softmax warp out of it
+  static constexpr int kStages = (H == 128) ? 3 : (kMaskStage ? 6 : 10);
   // additive-mask staging: per softmax warp its 32 rows x 128 16-bit columns, 16-byte chunks
   // of row r swizzled by r mod 16
   static constexpr int kMaskWarpBytes = 32 * kBN * 2;
   static constexpr int kMaskOff = kKVOff + kStages * kKVTile;
   static constexpr int kMaskBytes = kMaskStage ? 4 * kQT * kMaskWarpBytes : 0;
   static constexpr int kSmem = kMaskOff + kMaskBytes + 1024;   // + alignment slack
+  static_assert(kSmem <= 232448, "shared memory");
   // Tensor memory: S_X (128 columns each), O_X (H columns each) and P_X (16-bit, two per
   // column: 64 columns).  With H = 128 there is no room for P: P_X overwrites the first 64
   // columns of S_X once S_X is in registers.
@@ -106,7 +110,11 @@ struct Cfg {
 };
 
 struct TcArgs {
-  int B, Nq, Nkv, S, T, group, nunits;
+  int B, Nq, Nkv, S, T, group;
+  int nunits;                                       // work units (two query tiles each)
+  int nrow;                                         // row blocks per (batch, head or head pair)
+  int pairs;                                        // units per (batch, kv head, row block)
+  int head_pairs;                                   // 1: the tiles of a unit are two heads of a group
   float scale, scale_log2, cap_in, cap_out_log2;   // cap_* used when softcap > 0
   int has_softcap;
   int cap_fixed;                                    // bf16 softcap: fixed row maximum (below)
@@ -124,6 +132,7 @@ struct TcArgs {
   int q_ds, q_dn, q_db, kv_ds, kv_dn, kv_db;        // tensor-map dimension of seq / head / batch
   void* y;                                          // NULL: y is not written (statistics only)
   int64_t y_sb, y_sh, y_ss;
+  int y_ds, y_dn, y_db;                             // tensor-map dimension of seq / head / batch of y
   // Row statistics for the backward pass (one thread per row only): the log2-sum-exp of the
   // row in units of q.k scale log2(e), and delta = dY . O (O normalised, fp32), indexed
   // (b * Nq + h) * S + i.  NULL: not written.
@@ -308,21 +317,64 @@ __device__ __forceinline__ void keep_bits128(const void* row, bool is_u8, int k0
   }
 }
 
-template <int H, bool kBF16, int kMode, int QT, int SPLIT, bool kStats>
-__global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>::kMinBlocks)
+// Work unit: two 128-row query tiles (0, 1) that stream the same key/value tiles of one kv
+// head.  With an even group they are two query heads of the group over the same rows (same
+// key range, same structural rules); otherwise two consecutive row blocks of one head.
+struct Unit {
+  int b, kvh;
+  int qh[2];          // query head of each tile
+  int m[2];           // first query row of each tile
+  int kv_t0, n_tiles; // key tiles some row of the unit admits
+  int64_t len_b;
+};
+
+// k-th unit of CTA c among G: units are numbered heavy first and dealt round by round, the
+// direction alternating (0..G-1, then G-1..0, ...), which balances the causal rows' costs.
+__device__ __forceinline__ int unit_at(int k, int c, int G) { return k * G + ((k & 1) ? (G - 1 - c) : c); }
+
+__device__ __forceinline__ void decode_unit(const TcArgs& a, int u, Unit& w) {
+  int t = u;
+  const int g = t % a.pairs; t /= a.pairs;
+  w.kvh = t % a.Nkv; t /= a.Nkv;
+  w.b = t % a.B; t /= a.B;
+  const int ru = a.nrow - 1 - t;   // unit 0 takes the last (heaviest) row block
+  if (a.head_pairs) {
+    w.qh[0] = w.kvh * a.group + 2 * g;
+    w.qh[1] = w.qh[0] + 1;
+    w.m[0] = w.m[1] = ru * kBM;
+  } else {
+    w.qh[0] = w.qh[1] = w.kvh * a.group + g;
+    w.m[0] = ru * 2 * kBM;
+    w.m[1] = w.m[0] + kBM;
+  }
+  w.len_b = lens_of(a, w.b);
+  const int last = min(a.S, w.m[1] + kBM) - 1;
+  int64_t lo_f, hi_f, lo_l, hi_l;
+  key_bounds(a, w.len_b, w.m[0], lo_f, hi_f);
+  key_bounds(a, w.len_b, last, lo_l, hi_l);
+  const int64_t lo_key = max64(0, min64(lo_f, lo_l));
+  const int64_t hi_key = min64((int64_t)a.T - 1, max64(hi_f, hi_l));
+  w.kv_t0 = (int)(lo_key / kBN);
+  w.n_tiles = (hi_key >= lo_key) ? (int)(hi_key / kBN) - w.kv_t0 + 1 : 0;
+}
+
+template <int H, bool kBF16, int kMode, int SPLIT, bool kStats>
+__global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                      const __grid_constant__ CUtensorMap tv, const TcArgs a) {
-  constexpr bool kStage = (kMode == kAddMask) && (SPLIT == 1);   // additive mask through shared memory
-  using C = Cfg<H, QT, kStage>;
-  using Lay = Layout<QT, SPLIT>;
-  constexpr int kQT = QT;
+                      const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap ty,
+                      const TcArgs a) {
+  // additive mask through shared memory (H = 64; H = 128 reads it per thread)
+  constexpr bool kStage = (kMode == kAddMask) && (SPLIT == 1) && (H == 64);
+  constexpr int kQT = 2;
+  using C = Cfg<H, kQT, kStage>;
+  using Lay = Layout<kQT, SPLIT>;
   constexpr int kSplit = SPLIT;                     // softmax threads per query row
   constexpr int kHalf = kBN / kSplit;               // score columns per softmax thread
   constexpr int kSmxThreads = Lay::kSmxThreads;
   using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_q, bar_qready, bar_drain;
+  __shared__ __align__(8) uint64_t bar_qfull[2], bar_ystaged[2], bar_qready, bar_drain;
   __shared__ __align__(8) uint64_t bar_full[C::kStages], bar_empty[C::kStages];
   __shared__ __align__(8) uint64_t bar_sfull[2], bar_sfree[2], bar_pfull[2], bar_odone[2];
   __shared__ uint32_t tmem_base_sh;
@@ -331,30 +383,15 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
   __shared__ float red_sum[kQT][kSplit][kSplit == 2 ? kBM : 1];      // [query tile][part][row]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // ---- work unit: (query-tile pair, batch, kv head, head within the group), heavy first
-  int t = blockIdx.x;
-  const int g_idx = t % a.group; t /= a.group;
-  const int kvh = t % a.Nkv; t /= a.Nkv;
-  const int b = t % a.B; t /= a.B;
-  const int unit = a.nunits - 1 - t;
-  const int qh = kvh * a.group + g_idx;
-  const int m0 = unit * kQT * kBM;
-  const int m1 = min(a.S, m0 + kQT * kBM);
-  const int64_t len_b = lens_of(a, b);
-
-  // key tiles any row of this CTA can admit
-  int64_t lo_first, hi_first, lo_last, hi_last;
-  key_bounds(a, len_b, m0, lo_first, hi_first);
-  key_bounds(a, len_b, m1 - 1, lo_last, hi_last);
-  const int64_t lo_key = max64(0, min64(lo_first, lo_last));
-  const int64_t hi_key = min64((int64_t)a.T - 1, max64(hi_first, hi_last));
-  const int kv_t0 = (int)(lo_key / kBN);
-  const int n_tiles = (hi_key >= lo_key) ? (int)(hi_key / kBN) - kv_t0 + 1 : 0;
+  const int G = gridDim.x, cta = blockIdx.x;
+  // the Q tiles need a prologue pass (projection bias) before the first MMA reads them
+  const bool q_prologue = a.q_bias != nullptr;
 
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + C::kQOff, sKV = sbase + C::kKVOff;
-  const uint32_t b_q = smem_u32(&bar_q), b_qready = smem_u32(&bar_qready), b_drain = smem_u32(&bar_drain);
+  const uint32_t b_qready = smem_u32(&bar_qready), b_drain = smem_u32(&bar_drain);
+  auto b_qfull = [&](int q) { return smem_u32(&bar_qfull[q]); };
+  auto b_ystaged = [&](int q) { return smem_u32(&bar_ystaged[q]); };
   auto b_full = [&](int s) { return smem_u32(&bar_full[s]); };
   auto b_empty = [&](int s) { return smem_u32(&bar_empty[s]); };
   auto b_sfull = [&](int x) { return smem_u32(&bar_sfull[x]); };
@@ -366,7 +403,10 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    mbar_init(b_q, 1);
+    for (int q = 0; q < 2; ++q) {
+      mbar_init(b_qfull(q), 1);
+      mbar_init(b_ystaged(q), kSmxThreads);
+    }
     mbar_init(b_qready, kSmxThreads);
     mbar_init(b_drain, 1);
     for (int s = 0; s < C::kStages; ++s) { mbar_init(b_full(s), 1); mbar_init(b_empty(s), 1); }
@@ -389,28 +429,27 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
   // the control warpgroup hands registers to the softmax warpgroups
   if (warp < 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Lay::kCtlRegs));
 
-  // Ring order of the K/V tiles follows their first use by the MMA warp.  With P aliasing S
-  // (H = 128): K_0, V_0, K_1, V_1, ...  Otherwise S_X(j+1) is issued before PV_X(j), so the K
-  // tiles run one step ahead: K_0, K_1, V_0, K_2, V_1, ...
+  // Every role walks the same unit sequence and skips the units with no admitted key.
+  // Barrier phases are running counts over the CTA's lifetime.
   if (warp == 0) {
     // ================================================================ TMA producer
-    // (the whole warp runs the loop and one elected lane issues the copies)
-    if (n_tiles > 0) {
-      const uint32_t leader = elect_one();
-      if (leader) {
-        prefetch_tmap(&tq);
-        prefetch_tmap(&tk);
-        prefetch_tmap(&tv);
-        int c1, c2, c3;
-        mbar_arrive_expect_tx(b_q, kQT * C::kQTile);
-        for (int x = 0; x < kQT; ++x) {
-          perm_coords(a.q_ds, a.q_dn, a.q_db, m0 + x * kBM, qh, b, c1, c2, c3);
-          for (int r = 0; r < C::kRegions; ++r)
-            tma_load_4d(sQ + x * C::kQTile + r * C::kRegionBytes, &tq, b_q, 64 * r, c1, c2, c3);
-        }
-      }
-      int seq = 0;
-      bool ok = true;
+    // (the whole warp runs the loop and one elected lane issues the copies).  Ring order of
+    // the K/V tiles follows their first use by the MMA warp: with P aliasing S (H = 128)
+    // K_0, V_0, K_1, V_1, ...; otherwise S(j+1) is issued before PV(j), so the K tiles run one
+    // step ahead: K_0, K_1, V_0, K_2, V_1, ...
+    const uint32_t leader = elect_one();
+    if (leader) {
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+    }
+    int seq = 0;
+    bool ok = true;
+    for (int ku = 0; ok; ++ku) {
+      const int u = unit_at(ku, cta, G);
+      if (u >= a.nunits) break;
+      Unit w;
+      decode_unit(a, u, w);
+      if (w.n_tiles == 0) continue;
       auto load = [&](const CUtensorMap* map, int tile) -> bool {
         const int st = seq % C::kStages;
         if (seq >= C::kStages &&
@@ -419,7 +458,7 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
         if (leader) {
           mbar_arrive_expect_tx(b_full(st), C::kKVTile);
           int d1, d2, d3;
-          perm_coords(a.kv_ds, a.kv_dn, a.kv_db, (kv_t0 + tile) * kBN, kvh, b, d1, d2, d3);
+          perm_coords(a.kv_ds, a.kv_dn, a.kv_db, (w.kv_t0 + tile) * kBN, w.kvh, w.b, d1, d2, d3);
           for (int r = 0; r < C::kRegions; ++r)
             tma_load_4d(sKV + st * C::kKVTile + r * C::kRegionBytes, map, b_full(st), 64 * r, d1, d2, d3);
         }
@@ -427,89 +466,180 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
         return true;
       };
       ok = load(&tk, 0);
-      for (int j = 0; j < n_tiles && ok; ++j) {
+      for (int j = 0; j < w.n_tiles && ok; ++j) {
         if constexpr (C::kAlias) {
           ok = load(&tv, j);
-          if (ok && j + 1 < n_tiles) ok = load(&tk, j + 1);
+          if (ok && j + 1 < w.n_tiles) ok = load(&tk, j + 1);
         } else {
-          if (j + 1 < n_tiles) ok = load(&tk, j + 1);
+          if (j + 1 < w.n_tiles) ok = load(&tk, j + 1);
           if (ok) ok = load(&tv, j);
         }
       }
-      if (__any_sync(0xffffffffu, !ok || *abortp)) {
-        // some role gave up: let every copy already issued land before the CTA can exit
-        mbar_wait_bounded(b_q, 0, nullptr, kDrainNs);
-        for (int s = 0; s < C::kStages && s < seq; ++s) {
-          const int last = s + ((seq - 1 - s) / C::kStages) * C::kStages;
-          mbar_wait_bounded(b_full(s), (last / C::kStages) & 1, nullptr, kDrainNs);
+    }
+    if (__any_sync(0xffffffffu, !ok || *abortp)) {
+      // some role gave up: let every copy already issued land before the CTA can exit
+      for (int s = 0; s < C::kStages && s < seq; ++s) {
+        const int last = s + ((seq - 1 - s) / C::kStages) * C::kStages;
+        mbar_wait_bounded(b_full(s), (last / C::kStages) & 1, nullptr, kDrainNs);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 2) {
+    // ================================================================ Q loads, y stores
+    // Unit k (k-th unit with work) uses Q buffer k % 2.  The next unit's Q tiles load while
+    // the current unit runs; once a unit's softmax warps have staged its output y in the
+    // buffer (its last PV, and with it every MMA that read Q, is complete), this warp stores
+    // y by TMA, waits until the stores have read the buffer and loads the Q tiles of unit
+    // k + 2 into it.
+    const uint32_t leader = elect_one();
+    if (leader) {
+      prefetch_tmap(&tq);
+      if (a.y) prefetch_tmap(&ty);
+    }
+    int kq = 0;                     // unit cursor of the Q loads
+    int nload[2] = {0, 0};          // Q loads issued into each buffer
+    Unit wb0, wb1;                  // the unit whose Q (then y) each buffer holds
+    auto next_unit = [&](Unit& w) -> bool {
+      for (;; ++kq) {
+        const int u = unit_at(kq, cta, G);
+        if (u >= a.nunits) return false;
+        decode_unit(a, u, w);
+        if (w.n_tiles > 0) { ++kq; return true; }
+      }
+    };
+    auto load_q = [&](int q, const Unit& w) {
+      if (leader) {
+        mbar_arrive_expect_tx(b_qfull(q), kQT * C::kQTile);
+        for (int x = 0; x < kQT; ++x) {
+          int c1, c2, c3;
+          perm_coords(a.q_ds, a.q_dn, a.q_db, w.m[x], w.qh[x], w.b, c1, c2, c3);
+          for (int r = 0; r < C::kRegions; ++r)
+            tma_load_4d(sQ + q * C::kQBuf + x * C::kQTile + r * C::kRegionBytes, &tq, b_qfull(q), 64 * r, c1, c2, c3);
         }
       }
+      ++nload[q];
+    };
+    int loaded = 0;
+    if (next_unit(wb0)) { load_q(0, wb0); ++loaded; }
+    if (loaded == 1 && next_unit(wb1)) { load_q(1, wb1); ++loaded; }
+    bool ok = true;
+    for (int it = 0; it < loaded; ++it) {
+      const int q = it & 1;
+      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_ystaged(q), (it >> 1) & 1, abortp, a.wait_ns)))) break;
+      const Unit& w = q ? wb1 : wb0;
+      if (a.y && leader) {
+        for (int x = 0; x < kQT; ++x) {
+          if (w.m[x] >= a.S) continue;   // a second row block past the end of the queries
+          int c1, c2, c3;
+          perm_coords(a.y_ds, a.y_dn, a.y_db, w.m[x], w.qh[x], w.b, c1, c2, c3);
+          for (int r = 0; r < C::kRegions; ++r)
+            tma_store_4d(&ty, sQ + q * C::kQBuf + x * C::kQTile + r * C::kRegionBytes, 64 * r, c1, c2, c3);
+        }
+        bulk_commit();
+      }
+      if (leader) bulk_wait_read<0>();
+      __syncwarp();
+      Unit wn;
+      if (next_unit(wn)) {
+        if (q) wb1 = wn; else wb0 = wn;
+        load_q(q, wn);
+        ++loaded;
+      }
+    }
+    if (leader) bulk_wait_all();
+    if (__any_sync(0xffffffffu, !ok || *abortp)) {
+      // let every Q load already issued land before the CTA can exit
+      for (int q = 0; q < 2; ++q)
+        if (nload[q] > 0) mbar_wait_bounded(b_qfull(q), (nload[q] - 1) & 1, nullptr, kDrainNs);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ================================================================ MMA issuer
     // (the whole warp runs the loop; one elected lane issues every MMA and every commit, as a
     // commit tracks the MMAs of the thread that issues it)
-    if (n_tiles > 0) {
-      const uint32_t leader = elect_one();
-      auto commit = [&](uint32_t bar) {
-        if (leader) mma_commit(bar);
-      };
-      auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
-        return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abortp, a.wait_ns));
-      };
-      constexpr uint32_t kIdQK = idesc_f16(kBF16, kBM, kBN, false);
-      constexpr uint32_t kIdPV = idesc_f16(kBF16, kBM, H, true);
-      const uint32_t tS[2] = {tmem + C::kTmemS0, tmem + C::kTmemS1};   // [1] unused with one tile
-      const uint32_t tO[2] = {tmem + C::kTmemO0, tmem + C::kTmemO1};
-      const uint32_t tP[2] = {tmem + C::kTmemP0, tmem + C::kTmemP1};
-      int seq = 0;
-      auto wait_full = [&](int sq) -> bool {
-        const bool ok = wait_all(b_full(sq % C::kStages), (sq / C::kStages) & 1);
-        tc_fence_after();
-        return ok;
-      };
-      // descriptors differ only in their start-address field: build them once
-      const uint64_t dQ[2] = {desc_sw128(sQ, 16, 1024), desc_sw128(sQ + C::kQTile, 16, 1024)};
-      const uint64_t dK0 = desc_sw128(sKV, 16, 1024);
-      const uint64_t dV0 = desc_sw128(sKV, C::kRegionBytes, 1024);
-      auto issue_S = [&](int x, int st) {
-        const uint64_t dk = dK0 + (uint64_t)((st * C::kKVTile) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < H / 16; ++kk) {
-          const uint64_t off = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
-          if (leader) mma_f16_ss(tS[x], dQ[x] + off, dk + off, kIdQK, kk > 0);
-        }
-      };
-      auto issue_PV = [&](int x, int st, bool acc) {
-        const uint64_t dv = dV0 + (uint64_t)((st * C::kKVTile) >> 4);
-#pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk)
-          if (leader) mma_f16_ts(tO[x], tP[x] + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdPV, (acc || kk > 0) ? 1u : 0u);
-      };
-      bool ok = wait_all(a.q_bias ? b_qready : b_q, 0);
+    const uint32_t leader = elect_one();
+    auto commit = [&](uint32_t bar) {
+      if (leader) mma_commit(bar);
+    };
+    auto wait_all = [&](uint32_t bar, uint32_t parity) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abortp, a.wait_ns));
+    };
+    constexpr uint32_t kIdQK = idesc_f16(kBF16, kBM, kBN, false);
+    constexpr uint32_t kIdPV = idesc_f16(kBF16, kBM, H, true);
+    const uint32_t tS[2] = {tmem + C::kTmemS0, tmem + C::kTmemS1};
+    const uint32_t tO[2] = {tmem + C::kTmemO0, tmem + C::kTmemO1};
+    const uint32_t tP[2] = {tmem + C::kTmemP0, tmem + C::kTmemP1};
+    int seq = 0, it = 0;
+    int ns = 0;   // S batches issued (each covers both tiles)
+    int np = 0;   // P batches consumed (each covers both tiles)
+    auto wait_full = [&](int sq) -> bool {
+      const bool ok = wait_all(b_full(sq % C::kStages), (sq / C::kStages) & 1);
       tc_fence_after();
-      if (ok) ok = wait_full(seq);
-      if (ok) {
+      return ok;
+    };
+    // descriptors differ only in their start-address field: build them once (Q: buffer 0)
+    const uint64_t dQ[2] = {desc_sw128(sQ, 16, 1024), desc_sw128(sQ + C::kQTile, 16, 1024)};
+    uint64_t qoff = 0;   // start-address offset of the current unit's Q buffer
+    const uint64_t dK0 = desc_sw128(sKV, 16, 1024);
+    const uint64_t dV0 = desc_sw128(sKV, C::kRegionBytes, 1024);
+    auto issue_S = [&](int x, int st) {
+      const uint64_t dk = dK0 + (uint64_t)((st * C::kKVTile) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < H / 16; ++kk) {
+        const uint64_t off = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
+        if (leader) mma_f16_ss(tS[x], dQ[x] + qoff + off, dk + off, kIdQK, kk > 0);
+      }
+    };
+    auto issue_PV = [&](int x, int st, bool acc) {
+      const uint64_t dv = dV0 + (uint64_t)((st * C::kKVTile) >> 4);
+#pragma unroll
+      for (int kk = 0; kk < kBN / 16; ++kk)
+        if (leader) mma_f16_ts(tO[x], tP[x] + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdPV, (acc || kk > 0) ? 1u : 0u);
+    };
+    // S_x may be overwritten once softmax x has taken the previous S_x into registers (with
+    // P aliasing S, the in-order PV_x that read P_x already implies it)
+    auto wait_sfree = [&](int x) -> bool {
+      if (C::kAlias || ns == 0) return true;
+      const bool ok = wait_all(b_sfree(x), (ns - 1) & 1);
+      tc_fence_after();
+      return ok;
+    };
+    bool ok = true;
+    for (int ku = 0; ok; ++ku) {
+      const int u = unit_at(ku, cta, G);
+      if (u >= a.nunits) break;
+      Unit w;
+      decode_unit(a, u, w);
+      const int n = w.n_tiles;
+      if (n == 0) continue;
+      if (!(ok = wait_all(q_prologue ? b_qready : b_qfull(it & 1), q_prologue ? (it & 1) : ((it >> 1) & 1)))) break;
+      tc_fence_after();
+      qoff = (uint64_t)(((it & 1) * C::kQBuf) >> 4);
+      ++it;
+      if (!(ok = wait_full(seq))) break;
+      {
         const int st = seq % C::kStages;
-        for (int x = 0; x < kQT; ++x) {
+        for (int x = 0; x < kQT && ok; ++x) {
+          if (!(ok = wait_sfree(x))) break;
           issue_S(x, st);
           commit(b_sfull(x));
         }
+        if (!ok) break;
+        ++ns;
         commit(b_empty(st));
         ++seq;
       }
       if constexpr (C::kAlias) {
         // P_X(j) lives in S_X's columns: PV_X(j) first, then S_X(j+1); one commit on
         // sfull_X then also tells softmax X that O_X holds PV_X(j)
-        for (int j = 0; j < n_tiles && ok; ++j) {
-          const bool more = j + 1 < n_tiles;
+        for (int j = 0; j < n && ok; ++j) {
+          const bool more = j + 1 < n;
           const int vst = seq % C::kStages;
           if (!(ok = wait_full(seq))) break;
           ++seq;
           const int kst = seq % C::kStages;
           for (int x = 0; x < kQT && ok; ++x) {
-            if (!(ok = wait_all(b_pfull(x), j & 1))) break;
+            if (!(ok = wait_all(b_pfull(x), np & 1))) break;
             tc_fence_after();
             issue_PV(x, vst, j > 0);
             if (more) {
@@ -519,6 +649,8 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
             commit(b_sfull(x));
           }
           if (!ok) break;
+          ++np;
+          if (more) ++ns;
           commit(b_empty(vst));
           if (more) {
             commit(b_empty(kst));
@@ -526,441 +658,464 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
           }
         }
       } else {
-        for (int j = 0; j < n_tiles && ok; ++j) {
-          if (j + 1 < n_tiles) {
+        for (int j = 0; j < n && ok; ++j) {
+          if (j + 1 < n) {
             // S_X(j+1) as soon as softmax X has taken S_X(j) out of tensor memory
             const int kst = seq % C::kStages;
             if (!(ok = wait_full(seq))) break;
             ++seq;
             for (int x = 0; x < kQT && ok; ++x) {
-              if (!(ok = wait_all(b_sfree(x), j & 1))) break;
-              tc_fence_after();
+              if (!(ok = wait_sfree(x))) break;
               issue_S(x, kst);
               commit(b_sfull(x));
             }
             if (!ok) break;
+            ++ns;
             commit(b_empty(kst));
           }
           const int vst = seq % C::kStages;
           if (!(ok = wait_full(seq))) break;
           ++seq;
           for (int x = 0; x < kQT && ok; ++x) {
-            if (!(ok = wait_all(b_pfull(x), j & 1))) break;
+            if (!(ok = wait_all(b_pfull(x), np & 1))) break;
             tc_fence_after();
             issue_PV(x, vst, j > 0);
             commit(b_odone(x));
           }
           if (!ok) break;
+          ++np;
           commit(b_empty(vst));
         }
       }
-      // every MMA this thread issued completes before the CTA frees its tensor memory
-      commit(b_drain);
-      mbar_wait_bounded(b_drain, 0, nullptr, kDrainNs);
     }
+    // every MMA this thread issued completes before the CTA frees its tensor memory
+    commit(b_drain);
+    mbar_wait_bounded(b_drain, 0, nullptr, kDrainNs);
     __syncwarp();
   } else if (warp >= 4) {
     // ================================================================ softmax warpgroups
-    // Four warpgroups: (query tile A or B) x (score columns 0-63 or 64-127).  The two
-    // threads that share a row exchange their partial maxima through shared memory.
+    // (query tile 0 or 1) x (column part): one thread per row and part
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Lay::kSmxRegs));
     const int g = (warp - 4) >> 2;
-    const int x = g / kSplit;                       // query tile A or B
+    const int x = g / kSplit;                       // query tile
     const int hh = g % kSplit;                      // column part
     const int sub = warp & 3;                       // TMEM sub-partition of this warp
     const int row = sub * 32 + lane;                // row in the tile == TMEM lane
-    const int pair_bar = 1 + x * 4 + sub;           // named barrier of the two warps of these rows
-    const int64_t i = (int64_t)m0 + x * kBM + row;  // query row
-    const bool valid = i < a.S;
-    int64_t lo = 1, hi = 0;
-    if (valid) key_bounds(a, len_b, i, lo, hi);
-    // T <= 2^30, so the bounds fit 32 bits once clamped to [-1, T]
-    const int lo32 = (int)max64(-1, min64(lo, a.T));
-    const int hi32 = (int)max64(-1, min64(hi, a.T));
-    RowCtx ctx;
-    ctx.len = len_b;
-    ctx.pos = pos_of(a, len_b, i);
-    const void* mrow = nullptr;
-    if (kMode == kKeep && valid && a.r.keep_kind != SDPA_KEEP_NONE) {
-      const int esz = a.r.keep_kind == SDPA_KEEP_BOOL_U8 ? 1 : 4;
-      mrow = reinterpret_cast<const char*>(a.r.keep) +
-             (b * a.r.keep_sb + (int64_t)qh * a.r.keep_sh + i * a.r.keep_ss) * esz;
-    }
-    if (kMode == kAddMask && valid) {
-      const int esz = a.r.add_dtype == SDPA_F32 ? 4 : 2;
-      mrow = reinterpret_cast<const char*>(a.r.add) +
-             (b * a.r.add_sb + (int64_t)qh * a.r.add_sh + i * a.r.add_ss) * esz;
-    }
-    // staged mask: the warp's first row, the row stride and how many of its 32 rows exist
-    const int64_t wrow = (int64_t)m0 + x * kBM + sub * 32;
-    const char* mwarp = nullptr;
-    int mrows = 0;
-    const uint32_t sMask = sbase + C::kMaskOff + (uint32_t)(x * 4 + sub) * C::kMaskWarpBytes;
-    if (kStage && a.add_stage) {
-      mwarp = reinterpret_cast<const char*>(a.r.add) + (b * a.r.add_sb + (int64_t)qh * a.r.add_sh + wrow * a.r.add_ss) * 2;
-      mrows = (int)max64(0, min64(32, (int64_t)a.S - wrow));
-    }
+    const int pair_bar = 1 + x * 4 + sub;           // named barrier of the warps of these rows
     const uint32_t trow = tmem + ((uint32_t)(sub * 32) << 16);
     const uint32_t tS = trow + (x == 0 ? C::kTmemS0 : C::kTmemS1) + kHalf * hh;
     const uint32_t tO = trow + (x == 0 ? C::kTmemO0 : C::kTmemO1) + (H / kSplit) * hh;
     const uint32_t tP = trow + (x == 0 ? C::kTmemP0 : C::kTmemP1) + (kHalf / 2) * hh;
+    const uint32_t sMask = sbase + C::kMaskOff + (uint32_t)(x * 4 + sub) * C::kMaskWarpBytes;
     // log2-domain factor applied inside the exponent: raw scores (plain mode) carry the
     // scale or the softcap amplitude, additive-mask scores are in natural units, and the
     // generic mode produces log2-domain scores already
     const float kfac = (kMode == kPlain) ? (a.has_softcap ? a.cap_out_log2 : a.scale_log2)
                        : (kMode == kKeep) ? a.scale_log2
                                           : (kMode == kAddMask ? kLog2e : 1.f);
-    // kCapFixed: the fixed maximum (the cap, or the sink logit when that is larger)
-    float m_fixed = a.cap_out_log2;
-    if (kMode == kCapFixed && a.head_sink)
-      m_fixed = fmaxf(m_fixed, Elem<T>::to_f32(reinterpret_cast<const T*>(a.head_sink)[qh]) * kLog2e);
+    int cs = 0;   // sfull phases waited
+    int co = 0;   // odone phases waited
+    int it = 0;   // units with work
     bool ok = true;
+    for (int ku = 0; ok; ++ku) {
+      const int u = unit_at(ku, cta, G);
+      if (u >= a.nunits) break;
+      Unit w;
+      decode_unit(a, u, w);
+      const int n_tiles = w.n_tiles;
+      const int b = w.b;
+      const int qh = x == 0 ? w.qh[0] : w.qh[1];
+      const int mx0 = x == 0 ? w.m[0] : w.m[1];      // first row of this tile
+      const int64_t len_b = w.len_b;
+      const int64_t i = (int64_t)mx0 + row;          // query row
+      const bool valid = i < a.S;
+      int64_t lo = 1, hi = 0;
+      if (valid) key_bounds(a, len_b, i, lo, hi);
+      // T <= 2^30, so the bounds fit 32 bits once clamped to [-1, T]
+      const int lo32 = (int)max64(-1, min64(lo, a.T));
+      const int hi32 = (int)max64(-1, min64(hi, a.T));
+      RowCtx ctx;
+      ctx.len = len_b;
+      ctx.pos = pos_of(a, len_b, i);
+      const void* mrow = nullptr;
+      if (kMode == kKeep && valid && a.r.keep_kind != SDPA_KEEP_NONE) {
+        const int esz = a.r.keep_kind == SDPA_KEEP_BOOL_U8 ? 1 : 4;
+        mrow = reinterpret_cast<const char*>(a.r.keep) +
+               (b * a.r.keep_sb + (int64_t)qh * a.r.keep_sh + i * a.r.keep_ss) * esz;
+      }
+      if (kMode == kAddMask && valid) {
+        const int esz = a.r.add_dtype == SDPA_F32 ? 4 : 2;
+        mrow = reinterpret_cast<const char*>(a.r.add) +
+               (b * a.r.add_sb + (int64_t)qh * a.r.add_sh + i * a.r.add_ss) * esz;
+      }
+      // staged mask: the warp's first row, the row stride and how many of its 32 rows exist
+      const int64_t wrow = (int64_t)mx0 + sub * 32;
+      const char* mwarp = nullptr;
+      int mrows = 0;
+      if (kStage && a.add_stage) {
+        mwarp = reinterpret_cast<const char*>(a.r.add) + (b * a.r.add_sb + (int64_t)qh * a.r.add_sh + wrow * a.r.add_ss) * 2;
+        mrows = (int)max64(0, min64(32, (int64_t)a.S - wrow));
+      }
+      // kCapFixed: the fixed maximum (the cap, or the sink logit when that is larger)
+      float m_fixed = a.cap_out_log2;
+      if (kMode == kCapFixed && a.head_sink)
+        m_fixed = fmaxf(m_fixed, Elem<T>::to_f32(reinterpret_cast<const T*>(a.head_sink)[qh]) * kLog2e);
 
-    if (n_tiles > 0 && a.q_bias) {
-      // add the query segment of the projection bias to this row of Q (this thread's half
-      // of the columns) in shared memory
-      ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_q, 0, abortp, a.wait_ns));
-      if (ok) {
-        const uint32_t qRow = sQ + x * C::kQTile + row * 128;
-        const T* qb = reinterpret_cast<const T*>(a.q_bias) + (int64_t)qh * H;
-        const int swz = row & 7;
+      if (n_tiles > 0 && q_prologue) {
+        // add the query segment of the projection bias to this row of Q (this thread's part
+        // of the columns) in shared memory
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_qfull(it & 1), (it >> 1) & 1, abortp, a.wait_ns));
+        if (ok) {
+          const uint32_t qRow = sQ + (it & 1) * C::kQBuf + x * C::kQTile + row * 128;
+          const T* qb = reinterpret_cast<const T*>(a.q_bias) + (int64_t)qh * H;
+          const int swz = row & 7;
 #pragma unroll
-        for (int c16 = 0; c16 < H / (8 * kSplit); ++c16) {   // 16-byte chunks of this thread's part
-          const int cidx = hh * (H / (8 * kSplit)) + c16;      // chunk index within the row
-          const int r = cidx >> 3, c = cidx & 7;
-          const uint32_t addr = qRow + r * C::kRegionBytes + ((c ^ swz) << 4);
-          uint32_t w[4];
-          ld_shared_v4(addr, w[0], w[1], w[2], w[3]);
+          for (int c16 = 0; c16 < H / (8 * kSplit); ++c16) {   // 16-byte chunks of this thread's part
+            const int cidx = hh * (H / (8 * kSplit)) + c16;      // chunk index within the row
+            const int r = cidx >> 3, c = cidx & 7;
+            const uint32_t addr = qRow + r * C::kRegionBytes + ((c ^ swz) << 4);
+            uint32_t wv[4];
+            ld_shared_v4(addr, wv[0], wv[1], wv[2], wv[3]);
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int col = cidx * 8 + 2 * e;
-            const T* pv = reinterpret_cast<const T*>(&w[e]);
-            const float lo_f = Elem<T>::to_f32(pv[0]) + Elem<T>::to_f32(qb[col]);
-            const float hi_f = Elem<T>::to_f32(pv[1]) + Elem<T>::to_f32(qb[col + 1]);
-            w[e] = kBF16 ? pack_bf16x2(lo_f, hi_f) : pack_f16x2(lo_f, hi_f);
+            for (int e = 0; e < 4; ++e) {
+              const int col = cidx * 8 + 2 * e;
+              const T* pv = reinterpret_cast<const T*>(&wv[e]);
+              const float lo_f = Elem<T>::to_f32(pv[0]) + Elem<T>::to_f32(qb[col]);
+              const float hi_f = Elem<T>::to_f32(pv[1]) + Elem<T>::to_f32(qb[col + 1]);
+              wv[e] = kBF16 ? pack_bf16x2(lo_f, hi_f) : pack_f16x2(lo_f, hi_f);
+            }
+            st_shared_v4(addr, wv[0], wv[1], wv[2], wv[3]);
           }
-          st_shared_v4(addr, w[0], w[1], w[2], w[3]);
+          fence_proxy_async_smem();
         }
-        fence_proxy_async_smem();
+        mbar_arrive(b_qready);
+        if (!ok) break;
       }
-      mbar_arrive(b_qready);
-    }
+      const int qbuf = it & 1;   // this unit's Q buffer (units with work)
+      if (n_tiles > 0) ++it;
 
-    float m_use = (kMode == kCapFixed) ? m_fixed : -INFINITY, l = 0.f;
-    for (int j = 0; j < n_tiles && ok; ++j) {
-      bool staged = false;     // warp-uniform: the mask tile comes through shared memory
-      if constexpr (kStage) {
-        // copy the warp's mask rows for the tile now; the wait below hides the latency
-        const int k0 = (kv_t0 + j) * kBN;
-        staged = a.add_stage && (int64_t)k0 + kBN <= a.r.add_T;
-        if (staged) stage_mask_tile(sMask, mwarp + (int64_t)k0 * 2, a.r.add_ss * 2, mrows, a.add_vec, lane);
-      }
-      uint32_t kb[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};   // keep bits
-      if constexpr (kMode == kKeep) {
-        if (mrow)
-          keep_bits128(mrow, a.r.keep_kind == SDPA_KEEP_BOOL_U8, (kv_t0 + j) * kBN, a.r.keep_T, a.keep_vec != 0, kb);
-      }
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_sfull(x), j & 1, abortp, a.wait_ns)))) break;
-      tc_fence_after();
-      float s[kHalf];
-      {
-        uint32_t u[kHalf];
-#pragma unroll
-        for (int c = 0; c < kHalf / 32; ++c) tmem_ld32(tS + c * 32, u + c * 32);
-        tmem_ld_wait();
-#pragma unroll
-        for (int e = 0; e < kHalf; ++e) s[e] = __uint_as_float(u[e]);
-      }
-      if constexpr (!C::kAlias) {
-        // S_X(j) is in registers: the MMA warp may overwrite it with S_X(j+1)
-        tc_fence_before();
-        mbar_arrive(b_sfree(x));
-      }
-      if constexpr (kStage) {
-        if (staged) {
-          // the warp's copies have landed and are visible to every lane
-          ptx::cp_async_wait_all();
-          __syncwarp();
+      float m_use = (kMode == kCapFixed) ? m_fixed : -INFINITY, l = 0.f;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        bool staged = false;     // warp-uniform: the mask tile comes through shared memory
+        if constexpr (kStage) {
+          // copy the warp's mask rows for the tile now; the wait below hides the latency
+          const int k0 = (w.kv_t0 + j) * kBN;
+          staged = a.add_stage && (int64_t)k0 + kBN <= a.r.add_T;
+          if (staged) stage_mask_tile(sMask, mwarp + (int64_t)k0 * 2, a.r.add_ss * 2, mrows, a.add_vec, lane);
         }
-      }
+        uint32_t kb[4] = {0xffffffffu, 0xffffffffu, 0xffffffffu, 0xffffffffu};   // keep bits
+        if constexpr (kMode == kKeep) {
+          if (mrow)
+            keep_bits128(mrow, a.r.keep_kind == SDPA_KEEP_BOOL_U8, (w.kv_t0 + j) * kBN, a.r.keep_T, a.keep_vec != 0, kb);
+        }
+        if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_sfull(x), cs & 1, abortp, a.wait_ns)))) break;
+        ++cs;
+        tc_fence_after();
+        float s[kHalf];
+        {
+          uint32_t uu[kHalf];
+#pragma unroll
+          for (int c = 0; c < kHalf / 32; ++c) tmem_ld32(tS + c * 32, uu + c * 32);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < kHalf; ++e) s[e] = __uint_as_float(uu[e]);
+        }
+        if constexpr (!C::kAlias) {
+          // S_X(j) is in registers: the MMA warp may overwrite it with S_X(j+1)
+          tc_fence_before();
+          mbar_arrive(b_sfree(x));
+        }
+        if constexpr (kStage) {
+          if (staged) {
+            // the warp's copies have landed and are visible to every lane
+            ptx::cp_async_wait_all();
+            __syncwarp();
+          }
+        }
 
-      const int key0 = (kv_t0 + j) * kBN + kHalf * hh;
-      bool have_mx = false;       // set when the transform already produced this half's max
-      float mx_own = -INFINITY;
-      bool weights = false;       // kCapFixed: s already holds the weights p
-      if constexpr (kMode == kCapFixed) {
-        // s = raw q.k; the exponent c log2e tanh(s scale / c) - m, from the cubic when every
-        // |s| of the segment is in its range (eight chains of three-input max of |s|)
-        float am8[8];
+        const int key0 = (w.kv_t0 + j) * kBN + kHalf * hh;
+        bool have_mx = false;       // set when the transform already produced this half's max
+        float mx_own = -INFINITY;
+        bool weights = false;       // kCapFixed: s already holds the weights p
+        if constexpr (kMode == kCapFixed) {
+          // s = raw q.k; the exponent c log2e tanh(s scale / c) - m, from the cubic when every
+          // |s| of the segment is in its range (eight chains of three-input max of |s|)
+          float am8[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) am8[k] = fmaxf(fabsf(s[k]), fabsf(s[k + 8]));
+          for (int k = 0; k < 8; ++k) am8[k] = fmaxf(fabsf(s[k]), fabsf(s[k + 8]));
 #pragma unroll
-        for (int e = 16; e < kHalf; e += 16)
+          for (int e = 16; e < kHalf; e += 16)
 #pragma unroll
-          for (int k = 0; k < 8; ++k) am8[k] = fmax3(am8[k], fabsf(s[e + k]), fabsf(s[e + 8 + k]));
-        const float amax = fmax3(fmax3(am8[0], am8[1], am8[2]), fmax3(am8[3], am8[4], am8[5]), fmaxf(am8[6], am8[7]));
-        const float negm = -m_use;
-        const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
-        if (amax <= a.fx_lim && full) {
-          // every key admitted: exponent and weight in one pass, in place
-          const f2_t ca = f2_pack(a.fx_a, a.fx_a), cb = f2_pack(a.fx_b, a.fx_b), nm2 = f2_pack(negm, negm);
-#pragma unroll
-          for (int e = 0; e < kHalf; e += 2) {
-            const f2_t x2 = f2_pack(s[e], s[e + 1]);
-            const f2_t tt = f2_fma(f2_mul(x2, x2), cb, ca);
-            float z0, z1;
-            f2_unpack(f2_fma(x2, tt, nm2), z0, z1);
-            s[e] = ex2_approx(z0);
-            s[e + 1] = ex2_approx(z1);
-          }
-          weights = true;
-        } else if (amax <= a.fx_lim) {
-          const f2_t ca = f2_pack(a.fx_a, a.fx_a), cb = f2_pack(a.fx_b, a.fx_b), nm2 = f2_pack(negm, negm);
-#pragma unroll
-          for (int e = 0; e < kHalf; e += 2) {
-            const f2_t x2 = f2_pack(s[e], s[e + 1]);
-            const f2_t tt = f2_fma(f2_mul(x2, x2), cb, ca);
-            f2_unpack(f2_fma(x2, tt, nm2), s[e], s[e + 1]);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < kHalf; ++e) s[e] = fmaf(a.cap_out_log2, tanh_approx(s[e] * a.cap_in), negm);
-        }
-        if (!full) {
-          const int elo = lo32 - key0, ehi = hi32 - key0;
-#pragma unroll
-          for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
-        }
-      } else if constexpr (kMode == kPlain) {
-        const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
-        if (a.has_softcap) {
-          const f2_t cin = f2_pack(a.cap_in, a.cap_in);
-#pragma unroll
-          for (int e = 0; e < kHalf; e += 2) f2_unpack(f2_mul(f2_pack(s[e], s[e + 1]), cin), s[e], s[e + 1]);
-          bool poly = false;
-          float umax = -INFINITY;
-          if (full) {
-            float hi8[4], lo8[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k) { hi8[k] = fmaxf(s[k], s[k + 4]); lo8[k] = fminf(s[k], s[k + 4]); }
-#pragma unroll
-            for (int e = 8; e < kHalf; e += 8)
-#pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                hi8[k] = fmax3(hi8[k], s[e + k], s[e + 4 + k]);
-                lo8[k] = fminf(lo8[k], fminf(s[e + k], s[e + 4 + k]));
-              }
-            umax = fmaxf(fmaxf(hi8[0], hi8[1]), fmaxf(hi8[2], hi8[3]));
-            const float umin = fminf(fminf(lo8[0], lo8[1]), fminf(lo8[2], lo8[3]));
-            poly = fmaxf(umax, -umin) <= kTanhPolyLimit;
-          }
-          if (poly) {
-            // small arguments: odd polynomial on the FMA pipe (monotonic here, so the
-            // maximum is the polynomial of the largest argument)
-            const f2_t a1 = f2_pack(kTanhA1, kTanhA1), a2 = f2_pack(kTanhA2, kTanhA2);
+            for (int k = 0; k < 8; ++k) am8[k] = fmax3(am8[k], fabsf(s[e + k]), fabsf(s[e + 8 + k]));
+          const float amax = fmax3(fmax3(am8[0], am8[1], am8[2]), fmax3(am8[3], am8[4], am8[5]), fmaxf(am8[6], am8[7]));
+          const float negm = -m_use;
+          const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
+          if (amax <= a.fx_lim && full) {
+            // every key admitted: exponent and weight in one pass, in place
+            const f2_t ca = f2_pack(a.fx_a, a.fx_a), cb = f2_pack(a.fx_b, a.fx_b), nm2 = f2_pack(negm, negm);
 #pragma unroll
             for (int e = 0; e < kHalf; e += 2) {
-              const f2_t uu = f2_pack(s[e], s[e + 1]);
-              const f2_t z = f2_mul(uu, uu);
-              const f2_t q = f2_fma(z, a2, a1);
-              f2_unpack(f2_fma(f2_mul(uu, z), q, uu), s[e], s[e + 1]);
+              const f2_t x2 = f2_pack(s[e], s[e + 1]);
+              const f2_t tt = f2_fma(f2_mul(x2, x2), cb, ca);
+              float z0, z1;
+              f2_unpack(f2_fma(x2, tt, nm2), z0, z1);
+              s[e] = ex2_approx(z0);
+              s[e + 1] = ex2_approx(z1);
             }
-            mx_own = tanh_poly(umax);
-            have_mx = true;
+            weights = true;
+          } else if (amax <= a.fx_lim) {
+            const f2_t ca = f2_pack(a.fx_a, a.fx_a), cb = f2_pack(a.fx_b, a.fx_b), nm2 = f2_pack(negm, negm);
+#pragma unroll
+            for (int e = 0; e < kHalf; e += 2) {
+              const f2_t x2 = f2_pack(s[e], s[e + 1]);
+              const f2_t tt = f2_fma(f2_mul(x2, x2), cb, ca);
+              f2_unpack(f2_fma(x2, tt, nm2), s[e], s[e + 1]);
+            }
           } else {
 #pragma unroll
-            for (int e = 0; e < kHalf; ++e) s[e] = tanh_approx(s[e]);
+            for (int e = 0; e < kHalf; ++e) s[e] = fmaf(a.cap_out_log2, tanh_approx(s[e] * a.cap_in), negm);
           }
-        }
-        if (!full) {
-          const int elo = lo32 - key0, ehi = hi32 - key0;
+          if (!full) {
+            const int elo = lo32 - key0, ehi = hi32 - key0;
 #pragma unroll
-          for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
-        }
-      } else if constexpr (kMode == kKeep) {
-        // raw scores: a key the keep mask drops is excluded (bool) or gets the filter value
-        // (binary), as does every key at or past a key-padding length; then the bounds
-        const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
-        const bool all_keep = (kb[0] & kb[1] & kb[2] & kb[3]) == 0xffffffffu;
-        const int len_e = (a.r.len_kind == SDPA_LEN_KEYLEN_I32) ? (int)max64(-1, min64(len_b - key0, kHalf)) : kHalf;
-        if (!__all_sync(0xffffffffu, full && all_keep && len_e >= kHalf)) {
-          const bool drop_excludes = a.r.keep_kind == SDPA_KEEP_BOOL_U8;
-          const float fr = a.filter_raw;
-          const int elo = lo32 - key0, ehi = hi32 - key0;
+            for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
+          }
+        } else if constexpr (kMode == kPlain) {
+          const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
+          if (a.has_softcap) {
+            const f2_t cin = f2_pack(a.cap_in, a.cap_in);
+#pragma unroll
+            for (int e = 0; e < kHalf; e += 2) f2_unpack(f2_mul(f2_pack(s[e], s[e + 1]), cin), s[e], s[e + 1]);
+            bool poly = false;
+            float umax = -INFINITY;
+            if (full) {
+              float hi8[4], lo8[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) { hi8[k] = fmaxf(s[k], s[k + 4]); lo8[k] = fminf(s[k], s[k + 4]); }
+#pragma unroll
+              for (int e = 8; e < kHalf; e += 8)
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  hi8[k] = fmax3(hi8[k], s[e + k], s[e + 4 + k]);
+                  lo8[k] = fminf(lo8[k], fminf(s[e + k], s[e + 4 + k]));
+                }
+              umax = fmaxf(fmaxf(hi8[0], hi8[1]), fmaxf(hi8[2], hi8[3]));
+              const float umin = fminf(fminf(lo8[0], lo8[1]), fminf(lo8[2], lo8[3]));
+              poly = fmaxf(umax, -umin) <= kTanhPolyLimit;
+            }
+            if (poly) {
+              // small arguments: odd polynomial on the FMA pipe (monotonic here, so the
+              // maximum is the polynomial of the largest argument)
+              const f2_t a1 = f2_pack(kTanhA1, kTanhA1), a2 = f2_pack(kTanhA2, kTanhA2);
+#pragma unroll
+              for (int e = 0; e < kHalf; e += 2) {
+                const f2_t uu = f2_pack(s[e], s[e + 1]);
+                const f2_t z = f2_mul(uu, uu);
+                const f2_t q = f2_fma(z, a2, a1);
+                f2_unpack(f2_fma(f2_mul(uu, z), q, uu), s[e], s[e + 1]);
+              }
+              mx_own = tanh_poly(umax);
+              have_mx = true;
+            } else {
+#pragma unroll
+              for (int e = 0; e < kHalf; ++e) s[e] = tanh_approx(s[e]);
+            }
+          }
+          if (!full) {
+            const int elo = lo32 - key0, ehi = hi32 - key0;
+#pragma unroll
+            for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
+          }
+        } else if constexpr (kMode == kKeep) {
+          // raw scores: a key the keep mask drops is excluded (bool) or gets the filter value
+          // (binary), as does every key at or past a key-padding length; then the bounds
+          const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
+          const bool all_keep = (kb[0] & kb[1] & kb[2] & kb[3]) == 0xffffffffu;
+          const int len_e = (a.r.len_kind == SDPA_LEN_KEYLEN_I32) ? (int)max64(-1, min64(len_b - key0, kHalf)) : kHalf;
+          if (!__all_sync(0xffffffffu, full && all_keep && len_e >= kHalf)) {
+            const bool drop_excludes = a.r.keep_kind == SDPA_KEEP_BOOL_U8;
+            const float fr = a.filter_raw;
+            const int elo = lo32 - key0, ehi = hi32 - key0;
+#pragma unroll
+            for (int e = 0; e < kHalf; ++e) {
+              float v = s[e];
+              if (!((kb[e >> 5] >> (e & 31)) & 1u)) v = drop_excludes ? -INFINITY : v + fr;
+              if (e >= len_e) v += fr;
+              s[e] = (e >= elo && e <= ehi) ? v : -INFINITY;
+            }
+          }
+        } else if constexpr (kMode == kAddMask) {
+          // additive mask / attention bias, then softcap (or the reverse), then the bounds;
+          // scores stay in natural units here (kfac carries log2 e).  The mask is read eight
+          // columns at a time: from the warp's staged rows, else from global memory.
+          static_assert(kSplit == 1, "the additive-mask mode covers 128 columns per thread");
+          auto run = [&](auto f) {
+            if (staged) {
+              const uint32_t rowp = sMask + lane * 256;
+#pragma unroll
+              for (int c = 0; c < kHalf / 8; ++c) {
+                uint32_t w[4];
+                ld_shared_v4(rowp + ((c ^ (lane & 15)) << 4), w[0], w[1], w[2], w[3]);
+                if (!valid) w[0] = w[1] = w[2] = w[3] = 0u;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) s[8 * c + k] = f(s[8 * c + k], mask_elem<T>(w, k));
+              }
+              __syncwarp();   // every lane has read its row: the region takes the next tile
+            } else {
+#pragma unroll
+              for (int c = 0; c < kHalf / 8; ++c) {
+                uint32_t w[4] = {0u, 0u, 0u, 0u};
+                if (valid) load_mask_chunk(reinterpret_cast<const T*>(mrow), key0 + 8 * c, a.r.add_T, a.add_vec, w);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) s[8 * c + k] = f(s[8 * c + k], mask_elem<T>(w, k));
+              }
+            }
+          };
+          if (!a.has_softcap) {
+            const float sc = a.scale;
+            run([sc](float sv, float mv) { return fmaf(sv, sc, mv); });
+          } else if (!a.r.softcap_before_bias) {
+            const float sc = a.scale, cap = a.r.softcap, cin = 1.f / a.r.softcap;
+            run([sc, cap, cin](float sv, float mv) {
+              const float v = fmaf(sv, sc, mv);
+              return (v == -INFINITY) ? v : cap * tanh_approx(v * cin);
+            });
+          } else {
+            const float cap = a.r.softcap, cin = a.cap_in;
+            run([cap, cin](float sv, float mv) { return fmaf(cap, tanh_approx(sv * cin), mv); });
+          }
+          if (!((lo32 <= key0) && (key0 + kHalf - 1 <= hi32))) {
+            const int elo = lo32 - key0, ehi = hi32 - key0;
+#pragma unroll
+            for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
+          }
+        } else {
 #pragma unroll
           for (int e = 0; e < kHalf; ++e) {
-            float v = s[e];
-            if (!((kb[e >> 5] >> (e & 31)) & 1u)) v = drop_excludes ? -INFINITY : v + fr;
-            if (e >= len_e) v += fr;
-            s[e] = (e >= elo && e <= ehi) ? v : -INFINITY;
+            const int key = key0 + e;
+            float v = -INFINITY;
+            if (key >= lo32 && key <= hi32)
+              v = generic_score(a.r, ctx, s[e] * a.scale, b, qh, (int)i, key) * kLog2e;
+            s[e] = v;
           }
         }
-      } else if constexpr (kMode == kAddMask) {
-        // additive mask / attention bias, then softcap (or the reverse), then the bounds;
-        // scores stay in natural units here (kfac carries log2 e).  The mask is read eight
-        // columns at a time: from the warp's staged rows, else from global memory.
-        static_assert(kSplit == 1, "the additive-mask mode covers 128 columns per thread");
-        auto run = [&](auto f) {
-          if (staged) {
-            const uint32_t rowp = sMask + lane * 256;
+
+        // row maximum: this half (eight chains of three-input max), then the partner's half
+        if (kMode != kCapFixed && !have_mx) {
+          float mx8[8];
 #pragma unroll
-            for (int c = 0; c < kHalf / 8; ++c) {
-              uint32_t w[4];
-              ld_shared_v4(rowp + ((c ^ (lane & 15)) << 4), w[0], w[1], w[2], w[3]);
-              if (!valid) w[0] = w[1] = w[2] = w[3] = 0u;
+          for (int k = 0; k < 8; ++k) mx8[k] = fmax3(s[k], s[k + 8], -INFINITY);
 #pragma unroll
-              for (int k = 0; k < 8; ++k) s[8 * c + k] = f(s[8 * c + k], mask_elem<T>(w, k));
-            }
-            __syncwarp();   // every lane has read its row: the region takes the next tile
-          } else {
+          for (int e = 16; e < kHalf; e += 16)
 #pragma unroll
-            for (int c = 0; c < kHalf / 8; ++c) {
-              uint32_t w[4] = {0u, 0u, 0u, 0u};
-              if (valid) load_mask_chunk(reinterpret_cast<const T*>(mrow), key0 + 8 * c, a.r.add_T, a.add_vec, w);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) s[8 * c + k] = f(s[8 * c + k], mask_elem<T>(w, k));
-            }
+            for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], s[e + k], s[e + 8 + k]);
+          mx_own = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
+        }
+        float mx = mx_own;
+        if constexpr (kSplit == 2) {
+          red_max[j & 1][x][hh][row] = mx_own;
+          named_bar_sync(pair_bar, 64);
+          mx = fmaxf(mx_own, red_max[j & 1][x][hh ^ 1][row]);
+        }
+
+        // move the running maximum only when it grows by more than 2^8 (both halves of a
+        // row see the same maxima, so they take the same decision)
+        bool need = false;
+        float corr = 1.f;
+        if constexpr (kMode != kCapFixed) {
+          const float m_tile = mx * kfac;
+          const float m_new = fmaxf(m_use, m_tile);
+          need = m_new > m_use + kRescaleThreshold;
+          if (need) {
+            corr = ex2_approx(m_use - m_new);
+            m_use = m_new;
           }
-        };
-        if (!a.has_softcap) {
-          const float sc = a.scale;
-          run([sc](float sv, float mv) { return fmaf(sv, sc, mv); });
-        } else if (!a.r.softcap_before_bias) {
-          const float sc = a.scale, cap = a.r.softcap, cin = 1.f / a.r.softcap;
-          run([sc, cap, cin](float sv, float mv) {
-            const float v = fmaf(sv, sc, mv);
-            return (v == -INFINITY) ? v : cap * tanh_approx(v * cin);
-          });
+        }
+        f2_t acc2[4] = {f2_zero(), f2_zero(), f2_zero(), f2_zero()};
+        uint32_t pw[kHalf / 2];
+        if constexpr (kMode == kCapFixed) {
+          // s holds the exponents (masked keys: -inf), or the weights already
+          if (!weights) {
+#pragma unroll
+            for (int e = 0; e < kHalf; ++e) s[e] = ex2_approx(s[e]);
+          }
+#pragma unroll
+          for (int e = 0; e < kHalf; e += 2) {
+            acc2[(e >> 1) & 3] = f2_add(acc2[(e >> 1) & 3], f2_pack(s[e], s[e + 1]));
+            pw[e >> 1] = pack_bf16x2(s[e], s[e + 1]);
+          }
         } else {
-          const float cap = a.r.softcap, cin = a.cap_in;
-          run([cap, cin](float sv, float mv) { return fmaf(cap, tanh_approx(sv * cin), mv); });
-        }
-        if (!((lo32 <= key0) && (key0 + kHalf - 1 <= hi32))) {
-          const int elo = lo32 - key0, ehi = hi32 - key0;
+          // rows with nothing admitted yet get exponent -inf, hence p = 0
+          const float negm = (m_use == -INFINITY) ? -INFINITY : -m_use;
+          const f2_t kf2 = f2_pack(kfac, kfac), nm2 = f2_pack(negm, negm);
 #pragma unroll
-          for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < kHalf; ++e) {
-          const int key = key0 + e;
-          float v = -INFINITY;
-          if (key >= lo32 && key <= hi32)
-            v = generic_score(a.r, ctx, s[e] * a.scale, b, qh, (int)i, key) * kLog2e;
-          s[e] = v;
-        }
-      }
-
-      // row maximum: this half (eight chains of three-input max), then the partner's half
-      if (kMode != kCapFixed && !have_mx) {
-        float mx8[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) mx8[k] = fmax3(s[k], s[k + 8], -INFINITY);
-#pragma unroll
-        for (int e = 16; e < kHalf; e += 16)
-#pragma unroll
-          for (int k = 0; k < 8; ++k) mx8[k] = fmax3(mx8[k], s[e + k], s[e + 8 + k]);
-        mx_own = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7]));
-      }
-      float mx = mx_own;
-      if constexpr (kSplit == 2) {
-        red_max[j & 1][x][hh][row] = mx_own;
-        named_bar_sync(pair_bar, 64);
-        mx = fmaxf(mx_own, red_max[j & 1][x][hh ^ 1][row]);
-      }
-
-      // move the running maximum only when it grows by more than 2^8 (both halves of a
-      // row see the same maxima, so they take the same decision)
-      bool need = false;
-      float corr = 1.f;
-      if constexpr (kMode != kCapFixed) {
-        const float m_tile = mx * kfac;
-        const float m_new = fmaxf(m_use, m_tile);
-        need = m_new > m_use + kRescaleThreshold;
-        if (need) {
-          corr = ex2_approx(m_use - m_new);
-          m_use = m_new;
-        }
-      }
-      f2_t acc2[4] = {f2_zero(), f2_zero(), f2_zero(), f2_zero()};
-      uint32_t pw[kHalf / 2];
-      if constexpr (kMode == kCapFixed) {
-        // s holds the exponents (masked keys: -inf), or the weights already
-        if (!weights) {
-#pragma unroll
-          for (int e = 0; e < kHalf; ++e) s[e] = ex2_approx(s[e]);
-        }
-#pragma unroll
-        for (int e = 0; e < kHalf; e += 2) {
-          acc2[(e >> 1) & 3] = f2_add(acc2[(e >> 1) & 3], f2_pack(s[e], s[e + 1]));
-          pw[e >> 1] = pack_bf16x2(s[e], s[e + 1]);
-        }
-      } else {
-        // rows with nothing admitted yet get exponent -inf, hence p = 0
-        const float negm = (m_use == -INFINITY) ? -INFINITY : -m_use;
-        const f2_t kf2 = f2_pack(kfac, kfac), nm2 = f2_pack(negm, negm);
-#pragma unroll
-        for (int e = 0; e < kHalf; e += 2) {
-          float z0, z1;
-          f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), kf2, nm2), z0, z1);
-          const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
-          acc2[(e >> 1) & 3] = f2_add(acc2[(e >> 1) & 3], f2_pack(p0, p1));
-          pw[e >> 1] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
-        }
-      }
-      float r0, r1, r2, r3, r4, r5, r6, r7;
-      f2_unpack(acc2[0], r0, r1);
-      f2_unpack(acc2[1], r2, r3);
-      f2_unpack(acc2[2], r4, r5);
-      f2_unpack(acc2[3], r6, r7);
-      l = l * corr + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
-
-      // PV_X(j-1) must be done: it reads P_X and accumulates into O_X (with P aliasing S,
-      // the sfull_X completion already implied it)
-      if (j > 0) {
-        if constexpr (!C::kAlias) {
-          if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_odone(x), (j - 1) & 1, abortp, a.wait_ns)))) break;
-          tc_fence_after();
-        }
-        if (kMode != kCapFixed && __any_sync(0xffffffffu, need)) {
-          // rescale this thread's half of its row of the accumulator (factor 1 for rows
-          // that kept their maximum)
-          const f2_t c2 = f2_pack(corr, corr);
-#pragma unroll
-          for (int c = 0; c < H / (32 * kSplit); ++c) {
-            uint32_t o[32];
-            tmem_ld32(tO + c * 32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; e += 2) {
-              float v0, v1;
-              f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), c2), v0, v1);
-              o[e] = __float_as_uint(v0);
-              o[e + 1] = __float_as_uint(v1);
-            }
-            tmem_st32(tO + c * 32, o);
+          for (int e = 0; e < kHalf; e += 2) {
+            float z0, z1;
+            f2_unpack(f2_fma(f2_pack(s[e], s[e + 1]), kf2, nm2), z0, z1);
+            const float p0 = ex2_approx(z0), p1 = ex2_approx(z1);
+            acc2[(e >> 1) & 3] = f2_add(acc2[(e >> 1) & 3], f2_pack(p0, p1));
+            pw[e >> 1] = kBF16 ? pack_bf16x2(p0, p1) : pack_f16x2(p0, p1);
           }
-          tmem_st_wait();
         }
-      }
-      // P_X(j) into tensor memory: lane = row, column c holds keys 2c and 2c+1
-#pragma unroll
-      for (int c = 0; c < kHalf / 64; ++c) tmem_st32(tP + c * 32, pw + c * 32);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(b_pfull(x));
-    }
-    // a loop left early may still have mask copies in flight into this warp's region
-    if constexpr (kStage) ptx::cp_async_wait_all();
+        float r0, r1, r2, r3, r4, r5, r6, r7;
+        f2_unpack(acc2[0], r0, r1);
+        f2_unpack(acc2[1], r2, r3);
+        f2_unpack(acc2[2], r4, r5);
+        f2_unpack(acc2[3], r6, r7);
+        l = l * corr + (((r0 + r1) + (r2 + r3)) + ((r4 + r5) + (r6 + r7)));
 
-    // ---- epilogue: O / (l + sink term), rounded once to the output type
-    if (ok && n_tiles > 0) {
-      if constexpr (C::kAlias)
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_sfull(x), n_tiles & 1, abortp, a.wait_ns));
-      else
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_odone(x), (n_tiles - 1) & 1, abortp, a.wait_ns));
-    }
-    if (ok) {
+        // PV_X(j-1) must be done: it reads P_X and accumulates into O_X (with P aliasing S,
+        // the sfull_X completion already implied it)
+        if (j > 0) {
+          if constexpr (!C::kAlias) {
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_odone(x), co & 1, abortp, a.wait_ns)))) break;
+            ++co;
+            tc_fence_after();
+          }
+          if (kMode != kCapFixed && __any_sync(0xffffffffu, need)) {
+            // rescale this thread's half of its row of the accumulator (factor 1 for rows
+            // that kept their maximum)
+            const f2_t c2 = f2_pack(corr, corr);
+#pragma unroll
+            for (int c = 0; c < H / (32 * kSplit); ++c) {
+              uint32_t o[32];
+              tmem_ld32(tO + c * 32, o);
+              tmem_ld_wait();
+#pragma unroll
+              for (int e = 0; e < 32; e += 2) {
+                float v0, v1;
+                f2_unpack(f2_mul(f2_pack(__uint_as_float(o[e]), __uint_as_float(o[e + 1])), c2), v0, v1);
+                o[e] = __float_as_uint(v0);
+                o[e + 1] = __float_as_uint(v1);
+              }
+              tmem_st32(tO + c * 32, o);
+            }
+            tmem_st_wait();
+          }
+        }
+        // P_X(j) into tensor memory: lane = row, column c holds keys 2c and 2c+1
+#pragma unroll
+        for (int c = 0; c < kHalf / 64; ++c) tmem_st32(tP + c * 32, pw + c * 32);
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(b_pfull(x));
+      }
+      // a loop left early may still have mask copies in flight into this warp's region
+      if constexpr (kStage) ptx::cp_async_wait_all();
+      if (!ok) break;
+
+      // ---- epilogue: O / (l + sink term), rounded once to the output type.  The last PV of
+      // the unit must be done (with P aliasing S, its sfull commit says so).
+      if (n_tiles > 0) {
+        if constexpr (C::kAlias) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_sfull(x), cs & 1, abortp, a.wait_ns));
+          ++cs;
+        } else {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_odone(x), co & 1, abortp, a.wait_ns));
+          ++co;
+        }
+        if (!ok) break;
+      }
       tc_fence_after();
       float denom = l;
       if constexpr (kSplit == 2) {
@@ -973,6 +1128,11 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
       const float inv = (denom > 0.f && m_use != -INFINITY) ? 1.f / denom : 0.f;
       T* yrow = reinterpret_cast<T*>(a.y) + (int64_t)b * a.y_sb + (int64_t)qh * a.y_sh + i * a.y_ss +
                 (H / kSplit) * hh;
+      // y: staged in this unit's Q buffer (row = TMEM lane, the Q tiles' 128-byte swizzle)
+      // for the TMA stores of warp 2; a unit with no admitted key writes its zero rows
+      // directly
+      const bool write_y = !kStats || a.y != nullptr;
+      const uint32_t sYrow = sQ + qbuf * C::kQBuf + x * C::kQTile + row * 128;
       constexpr bool stats = kStats && kSplit == 1;   // the backward's statistics pass
       const T* dyrow = stats ? reinterpret_cast<const T*>(a.dy) + (int64_t)b * a.dy_sb + (int64_t)qh * a.dy_sh +
                                    i * a.dy_ss
@@ -992,23 +1152,39 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
           // delta = dY . O with O = o / denom in fp32
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint4 u = *reinterpret_cast<const uint4*>(dyrow + c * 32 + q * 8);
-            const T* e8 = reinterpret_cast<const T*>(&u);
+            const uint4 uv = *reinterpret_cast<const uint4*>(dyrow + c * 32 + q * 8);
+            const T* e8 = reinterpret_cast<const T*>(&uv);
 #pragma unroll
             for (int e = 0; e < 8; ++e) delta = fmaf(Elem<T>::to_f32(e8[e]), __uint_as_float(o[q * 8 + e]) * inv, delta);
           }
         }
-        if (valid && (!kStats || a.y)) {
+        if (n_tiles > 0) {
+          if (write_y) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t wv[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float v0 = __uint_as_float(o[q * 8 + 2 * e]) * inv;
+                const float v1 = __uint_as_float(o[q * 8 + 2 * e + 1]) * inv;
+                wv[e] = kBF16 ? pack_bf16x2(v0, v1) : pack_f16x2(v0, v1);
+              }
+              const int col = (H / kSplit) * hh + c * 32 + q * 8;   // first column of the piece
+              const uint32_t addr = sYrow + (col >> 6) * C::kRegionBytes + ((((col & 63) >> 3) ^ (row & 7)) << 4);
+              st_shared_v4(addr, wv[0], wv[1], wv[2], wv[3]);
+            }
+          }
+        } else if (valid && write_y) {
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            uint32_t w[4];
+            uint32_t wv[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
               const float v0 = __uint_as_float(o[q * 8 + 2 * e]) * inv;
               const float v1 = __uint_as_float(o[q * 8 + 2 * e + 1]) * inv;
-              w[e] = kBF16 ? pack_bf16x2(v0, v1) : pack_f16x2(v0, v1);
+              wv[e] = kBF16 ? pack_bf16x2(v0, v1) : pack_f16x2(v0, v1);
             }
-            *reinterpret_cast<uint4*>(yrow + c * 32 + q * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(yrow + c * 32 + q * 8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
           }
         }
       }
@@ -1017,6 +1193,13 @@ __global__ void __launch_bounds__(Layout<QT, SPLIT>::kThreads, Layout<QT, SPLIT>
         a.lse2_out[r_idx] = (denom > 0.f && m_use != -INFINITY) ? m_use + log2f(denom) : INFINITY;
         a.delta_out[r_idx] = delta;
       }
+      if (n_tiles > 0) {
+        // y is in the buffer, visible to the TMA stores
+        fence_proxy_async_smem();
+        mbar_arrive(b_ystaged(qbuf));
+      }
+      // the epilogue's tensor-memory reads are complete before this thread's next P store,
+      // which the MMA warp waits for before the next unit's first PV overwrites O
     }
   }
 
@@ -1086,51 +1269,60 @@ uint64_t wait_limit_ns() {
   return v;
 }
 
-template <int H, bool kBF16, int kMode, int QT, int SPLIT, bool kStats = false>
-cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, TcArgs a,
-                        int64_t units_per_qt_row, cudaStream_t st) {
-  using C = Cfg<H, QT, (kMode == kAddMask) && (SPLIT == 1)>;
-  using Lay = Layout<QT, SPLIT>;
+int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+template <int H, bool kBF16, int kMode, int SPLIT, bool kStats = false>
+cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& ty,
+                        TcArgs a, cudaStream_t st) {
+  using C = Cfg<H, 2, (kMode == kAddMask) && (SPLIT == 1) && (H == 64)>;
+  using Lay = Layout<2, SPLIT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, kBF16, kMode, QT, SPLIT, kStats>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    C::kSmem);
+    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, kBF16, kMode, SPLIT, kStats>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     // the in-kernel register split assumes the block is launched with kLaunchRegs per
     // thread; with fewer, the softmax warps' request could never be met
     cudaFuncAttributes fa{};
-    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<H, kBF16, kMode, QT, SPLIT, kStats>);
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<H, kBF16, kMode, SPLIT, kStats>);
     if (attr_err == cudaSuccess && fa.numRegs < Lay::kLaunchRegs) attr_err = cudaErrorLaunchOutOfResources;
   });
   if (attr_err != cudaSuccess) return attr_err;
-  a.nunits = (a.S + QT * kBM - 1) / (QT * kBM);
-  const int64_t units = units_per_qt_row * a.nunits;
-  if (units > 0x7fffffff) return cudaErrorInvalidValue;
-  prefill_tc_kernel<H, kBF16, kMode, QT, SPLIT, kStats><<<(unsigned)units, Lay::kThreads, C::kSmem, st>>>(tq, tk, tv, a);
+  // persistent: at most one CTA per SM (the tensor memory of a CTA fills the SM's), each
+  // walking its share of the units
+  const int sms = sm_count();
+  if (sms <= 0) return cudaErrorInvalidDevice;
+  const int grid = std::min(a.nunits, sms);
+  prefill_tc_kernel<H, kBF16, kMode, SPLIT, kStats><<<(unsigned)grid, Lay::kThreads, C::kSmem, st>>>(tq, tk, tv, ty, a);
   count_launch(1);
   return cudaGetLastError();
 }
 
-// Plain rules run one 128-row tile per CTA (two CTAs per SM); the additive-mask and generic
-// paths, which need more registers per thread, run two tiles per CTA.
+// Rule modes (additive mask, keep masks, bf16 softcap with a fixed maximum, per-element
+// generic rules, plain interval rules), each a compile-time variant of the kernel.
 template <int H, bool kBF16>
-cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const TcArgs& a,
-                     int64_t heads_batches, cudaStream_t st) {
+cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& ty,
+                     const TcArgs& a, cudaStream_t st) {
   if (a.lse2_out) {
     // the backward's statistics pass, in the rule mode of the problem (no softcap: the
     // backward rejects it)
     if (a.has_softcap) return cudaErrorInvalidValue;
-    if (a.generic) return launch_mode<H, kBF16, kGeneric, 2, 1, true>(tq, tk, tv, a, heads_batches, st);
-    if (a.add_fast) return launch_mode<H, kBF16, kAddMask, 2, 1, true>(tq, tk, tv, a, heads_batches, st);
-    if (a.keep_fast) return launch_mode<H, kBF16, kKeep, 1, 1, true>(tq, tk, tv, a, heads_batches, st);
-    return launch_mode<H, kBF16, kPlain, 1, 1, true>(tq, tk, tv, a, heads_batches, st);
+    if (a.generic) return launch_mode<H, kBF16, kGeneric, 1, true>(tq, tk, tv, ty, a, st);
+    if (a.add_fast) return launch_mode<H, kBF16, kAddMask, 1, true>(tq, tk, tv, ty, a, st);
+    if (a.keep_fast) return launch_mode<H, kBF16, kKeep, 1, true>(tq, tk, tv, ty, a, st);
+    return launch_mode<H, kBF16, kPlain, 1, true>(tq, tk, tv, ty, a, st);
   }
-  if (a.generic) return launch_mode<H, kBF16, kGeneric, 2, 1>(tq, tk, tv, a, heads_batches, st);
-  if (a.keep_fast) return launch_mode<H, kBF16, kKeep, 1, 1>(tq, tk, tv, a, heads_batches, st);
-  if (a.add_fast) return launch_mode<H, kBF16, kAddMask, 2, 1>(tq, tk, tv, a, heads_batches, st);
+  if (a.generic) return launch_mode<H, kBF16, kGeneric, 1>(tq, tk, tv, ty, a, st);
+  if (a.keep_fast) return launch_mode<H, kBF16, kKeep, 1>(tq, tk, tv, ty, a, st);
+  if (a.add_fast) return launch_mode<H, kBF16, kAddMask, 1>(tq, tk, tv, ty, a, st);
   if constexpr (kBF16)
-    if (a.cap_fixed) return launch_mode<H, kBF16, kCapFixed, 1, 1>(tq, tk, tv, a, heads_batches, st);
-  return launch_mode<H, kBF16, kPlain, 1, 1>(tq, tk, tv, a, heads_batches, st);
+    if (a.cap_fixed) return launch_mode<H, kBF16, kCapFixed, 1>(tq, tk, tv, ty, a, st);
+  return launch_mode<H, kBF16, kPlain, 1>(tq, tk, tv, ty, a, st);
 }
 
 }  // namespace
@@ -1231,15 +1423,28 @@ cudaError_t launch_prefill_tc_stats(const Problem& p, sdpa_dtype dt, float* lse2
     return cudaErrorInvalidValue;
   int vds, vdn, vdb;
   if (!make_map(&tv, p.v, dt, p.B, p.Nkv, p.T, p.Hv, &vds, &vdn, &vdb)) return cudaErrorInvalidValue;
+
   if (vds != a.kv_ds || vdn != a.kv_dn || vdb != a.kv_db) return cudaErrorInvalidValue;   // k and v views differ in order
-  const int64_t units = (int64_t)p.B * p.Nkv * p.group;   // times the query units, per layout
+  // y: one 64-column x 128-row box per store; a statistics pass without y never stores and
+  // takes Q's map as a stand-in
+  CUtensorMap ty = tq;
+  if (p.y.p && !make_map(&ty, p.y, dt, p.B, p.Nq, p.S, p.Hv, &a.y_ds, &a.y_dn, &a.y_db, 128))
+    return cudaErrorInvalidValue;
+  // work units: two heads of a group over one row block when the group is even, else two
+  // consecutive row blocks of one head
+  a.head_pairs = (p.group % 2) == 0;
+  a.pairs = a.head_pairs ? p.group / 2 : p.group;
+  a.nrow = a.head_pairs ? (p.S + kBM - 1) / kBM : (p.S + 2 * kBM - 1) / (2 * kBM);
+  const int64_t units = (int64_t)a.nrow * p.B * p.Nkv * a.pairs;
+  if (units > 0x7fffffff) return cudaErrorInvalidValue;
+  a.nunits = (int)units;
   const bool bf = dt == SDPA_BF16;
   if (p.H == 128) {
     *name = bf ? "prefill_tc_bf16_h128" : "prefill_tc_f16_h128";
-    return bf ? launch_t<128, true>(tq, tk, tv, a, units, st) : launch_t<128, false>(tq, tk, tv, a, units, st);
+    return bf ? launch_t<128, true>(tq, tk, tv, ty, a, st) : launch_t<128, false>(tq, tk, tv, ty, a, st);
   }
   *name = bf ? "prefill_tc_bf16_h64" : "prefill_tc_f16_h64";
-  return bf ? launch_t<64, true>(tq, tk, tv, a, units, st) : launch_t<64, false>(tq, tk, tv, a, units, st);
+  return bf ? launch_t<64, true>(tq, tk, tv, ty, a, st) : launch_t<64, false>(tq, tk, tv, ty, a, st);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tc_encode_fn() { return encode_fn(); }
