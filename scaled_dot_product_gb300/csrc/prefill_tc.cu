@@ -864,21 +864,28 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
             }
             weights = true;
           } else if (amax <= a.fx_lim) {
+            // some keys excluded (the causal diagonal, a length boundary): the same single
+            // pass, an excluded key's exponent replaced by -inf (weight 0)
             const f2_t ca = f2_pack(a.fx_a, a.fx_a), cb = f2_pack(a.fx_b, a.fx_b), nm2 = f2_pack(negm, negm);
+            const int elo = lo32 - key0, ehi = hi32 - key0;
 #pragma unroll
             for (int e = 0; e < kHalf; e += 2) {
               const f2_t x2 = f2_pack(s[e], s[e + 1]);
               const f2_t tt = f2_fma(f2_mul(x2, x2), cb, ca);
-              f2_unpack(f2_fma(x2, tt, nm2), s[e], s[e + 1]);
+              float z0, z1;
+              f2_unpack(f2_fma(x2, tt, nm2), z0, z1);
+              s[e] = ex2_approx((e >= elo && e <= ehi) ? z0 : -INFINITY);
+              s[e + 1] = ex2_approx((e + 1 >= elo && e + 1 <= ehi) ? z1 : -INFINITY);
             }
+            weights = true;
           } else {
 #pragma unroll
             for (int e = 0; e < kHalf; ++e) s[e] = fmaf(a.cap_out_log2, tanh_approx(s[e] * a.cap_in), negm);
-          }
-          if (!full) {
-            const int elo = lo32 - key0, ehi = hi32 - key0;
+            if (!full) {
+              const int elo = lo32 - key0, ehi = hi32 - key0;
 #pragma unroll
-            for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
+              for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
+            }
           }
         } else if constexpr (kMode == kPlain) {
           const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
