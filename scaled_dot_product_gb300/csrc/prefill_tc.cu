@@ -83,20 +83,25 @@ struct Cfg {
   static constexpr int kRegionBytes = 128 * 128;       // 128 rows x 128 bytes
   static constexpr int kQTile = kBM * H * 2;
   static constexpr int kKVTile = kBN * H * 2;
-  // Q is double-buffered (the next unit's tiles load during the current unit); a finished
-  // unit's buffer then stages its output y for the TMA stores
+  // Q holds the unit's two tiles; the next unit's tiles load once the current unit's last S
+  // MMAs have read them
   static constexpr int kQBuf = kQT * kQTile;
   static constexpr int kQOff = 0;
-  static constexpr int kKVOff = 2 * kQBuf;
+  static constexpr int kKVOff = kQBuf;
   // K/V ring depth: what is left of the shared memory; a staged additive mask (H = 64 only)
   // takes 8 KB per softmax warp out of it
-  static constexpr int kStages = (H == 128) ? 3 : (kMaskStage ? 6 : 10);
+  static constexpr int kStages = (H == 128) ? 4 : (kMaskStage ? 6 : 10);
   // additive-mask staging: per softmax warp its 32 rows x 128 16-bit columns, 16-byte chunks
   // of row r swizzled by r mod 16
   static constexpr int kMaskWarpBytes = 32 * kBN * 2;
   static constexpr int kMaskOff = kKVOff + kStages * kKVTile;
   static constexpr int kMaskBytes = kMaskStage ? 4 * kQT * kMaskWarpBytes : 0;
-  static constexpr int kSmem = kMaskOff + kMaskBytes + 1024;   // + alignment slack
+  // output staging for the TMA stores of y: per softmax warp 32 rows x 64 columns (4 KB,
+  // 128-byte swizzle); the additive-mask mode reuses the warp's mask region
+  static constexpr int kYWarpBytes = 32 * 128;
+  static constexpr int kYOff = kMaskOff + kMaskBytes;
+  static constexpr int kYBytes = kMaskStage ? 0 : 4 * kQT * kYWarpBytes;
+  static constexpr int kSmem = kYOff + kYBytes + 1024;   // + alignment slack
   static_assert(kSmem <= 232448, "shared memory");
   // Tensor memory: S_X (128 columns each), O_X (H columns each) and P_X (16-bit, two per
   // column: 64 columns).  With H = 128 there is no room for P: P_X overwrites the first 64
@@ -374,7 +379,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
   using T = typename std::conditional<kBF16, __nv_bfloat16, __half>::type;
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t bar_qfull[2], bar_ystaged[2], bar_qready, bar_drain;
+  __shared__ __align__(8) uint64_t bar_qfull, bar_qempty, bar_qready, bar_drain;
   __shared__ __align__(8) uint64_t bar_full[C::kStages], bar_empty[C::kStages];
   __shared__ __align__(8) uint64_t bar_sfull[2], bar_sfree[2], bar_pfull[2], bar_odone[2];
   __shared__ uint32_t tmem_base_sh;
@@ -390,8 +395,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t sQ = sbase + C::kQOff, sKV = sbase + C::kKVOff;
   const uint32_t b_qready = smem_u32(&bar_qready), b_drain = smem_u32(&bar_drain);
-  auto b_qfull = [&](int q) { return smem_u32(&bar_qfull[q]); };
-  auto b_ystaged = [&](int q) { return smem_u32(&bar_ystaged[q]); };
+  const uint32_t b_qfull = smem_u32(&bar_qfull), b_qempty = smem_u32(&bar_qempty);
   auto b_full = [&](int s) { return smem_u32(&bar_full[s]); };
   auto b_empty = [&](int s) { return smem_u32(&bar_empty[s]); };
   auto b_sfull = [&](int x) { return smem_u32(&bar_sfull[x]); };
@@ -403,10 +407,8 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int q = 0; q < 2; ++q) {
-      mbar_init(b_qfull(q), 1);
-      mbar_init(b_ystaged(q), kSmxThreads);
-    }
+    mbar_init(b_qfull, 1);
+    mbar_init(b_qempty, 1);
     mbar_init(b_qready, kSmxThreads);
     mbar_init(b_drain, 1);
     for (int s = 0; s < C::kStages; ++s) { mbar_init(b_full(s), 1); mbar_init(b_empty(s), 1); }
@@ -439,10 +441,11 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
     // step ahead: K_0, K_1, V_0, K_2, V_1, ...
     const uint32_t leader = elect_one();
     if (leader) {
+      prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
     }
-    int seq = 0;
+    int seq = 0, it = 0;
     bool ok = true;
     for (int ku = 0; ok; ++ku) {
       const int u = unit_at(ku, cta, G);
@@ -465,7 +468,21 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
         ++seq;
         return true;
       };
+      // K_0 first: its ring slot frees up before the previous unit's last S MMAs have read Q
       ok = load(&tk, 0);
+      // the previous unit's last S MMAs have read its Q tiles
+      if (ok && it > 0) ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_qempty, (it - 1) & 1, abortp, a.wait_ns));
+      if (!ok) break;
+      if (leader) {
+        mbar_arrive_expect_tx(b_qfull, kQT * C::kQTile);
+        for (int x = 0; x < kQT; ++x) {
+          int c1, c2, c3;
+          perm_coords(a.q_ds, a.q_dn, a.q_db, w.m[x], w.qh[x], w.b, c1, c2, c3);
+          for (int r = 0; r < C::kRegions; ++r)
+            tma_load_4d(sQ + x * C::kQTile + r * C::kRegionBytes, &tq, b_qfull, 64 * r, c1, c2, c3);
+        }
+      }
+      ++it;
       for (int j = 0; j < w.n_tiles && ok; ++j) {
         if constexpr (C::kAlias) {
           ok = load(&tv, j);
@@ -478,79 +495,11 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
     }
     if (__any_sync(0xffffffffu, !ok || *abortp)) {
       // some role gave up: let every copy already issued land before the CTA can exit
+      if (it > 0) mbar_wait_bounded(b_qfull, (it - 1) & 1, nullptr, kDrainNs);
       for (int s = 0; s < C::kStages && s < seq; ++s) {
         const int last = s + ((seq - 1 - s) / C::kStages) * C::kStages;
         mbar_wait_bounded(b_full(s), (last / C::kStages) & 1, nullptr, kDrainNs);
       }
-    }
-    __syncwarp();
-  } else if (warp == 2) {
-    // ================================================================ Q loads, y stores
-    // Unit k (k-th unit with work) uses Q buffer k % 2.  The next unit's Q tiles load while
-    // the current unit runs; once a unit's softmax warps have staged its output y in the
-    // buffer (its last PV, and with it every MMA that read Q, is complete), this warp stores
-    // y by TMA, waits until the stores have read the buffer and loads the Q tiles of unit
-    // k + 2 into it.
-    const uint32_t leader = elect_one();
-    if (leader) {
-      prefetch_tmap(&tq);
-      if (a.y) prefetch_tmap(&ty);
-    }
-    int kq = 0;                     // unit cursor of the Q loads
-    int nload[2] = {0, 0};          // Q loads issued into each buffer
-    Unit wb0, wb1;                  // the unit whose Q (then y) each buffer holds
-    auto next_unit = [&](Unit& w) -> bool {
-      for (;; ++kq) {
-        const int u = unit_at(kq, cta, G);
-        if (u >= a.nunits) return false;
-        decode_unit(a, u, w);
-        if (w.n_tiles > 0) { ++kq; return true; }
-      }
-    };
-    auto load_q = [&](int q, const Unit& w) {
-      if (leader) {
-        mbar_arrive_expect_tx(b_qfull(q), kQT * C::kQTile);
-        for (int x = 0; x < kQT; ++x) {
-          int c1, c2, c3;
-          perm_coords(a.q_ds, a.q_dn, a.q_db, w.m[x], w.qh[x], w.b, c1, c2, c3);
-          for (int r = 0; r < C::kRegions; ++r)
-            tma_load_4d(sQ + q * C::kQBuf + x * C::kQTile + r * C::kRegionBytes, &tq, b_qfull(q), 64 * r, c1, c2, c3);
-        }
-      }
-      ++nload[q];
-    };
-    int loaded = 0;
-    if (next_unit(wb0)) { load_q(0, wb0); ++loaded; }
-    if (loaded == 1 && next_unit(wb1)) { load_q(1, wb1); ++loaded; }
-    bool ok = true;
-    for (int it = 0; it < loaded; ++it) {
-      const int q = it & 1;
-      if (!(ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_ystaged(q), (it >> 1) & 1, abortp, a.wait_ns)))) break;
-      const Unit& w = q ? wb1 : wb0;
-      if (a.y && leader) {
-        for (int x = 0; x < kQT; ++x) {
-          if (w.m[x] >= a.S) continue;   // a second row block past the end of the queries
-          int c1, c2, c3;
-          perm_coords(a.y_ds, a.y_dn, a.y_db, w.m[x], w.qh[x], w.b, c1, c2, c3);
-          for (int r = 0; r < C::kRegions; ++r)
-            tma_store_4d(&ty, sQ + q * C::kQBuf + x * C::kQTile + r * C::kRegionBytes, 64 * r, c1, c2, c3);
-        }
-        bulk_commit();
-      }
-      if (leader) bulk_wait_read<0>();
-      __syncwarp();
-      Unit wn;
-      if (next_unit(wn)) {
-        if (q) wb1 = wn; else wb0 = wn;
-        load_q(q, wn);
-        ++loaded;
-      }
-    }
-    if (leader) bulk_wait_all();
-    if (__any_sync(0xffffffffu, !ok || *abortp)) {
-      // let every Q load already issued land before the CTA can exit
-      for (int q = 0; q < 2; ++q)
-        if (nload[q] > 0) mbar_wait_bounded(b_qfull(q), (nload[q] - 1) & 1, nullptr, kDrainNs);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -577,9 +526,8 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
       tc_fence_after();
       return ok;
     };
-    // descriptors differ only in their start-address field: build them once (Q: buffer 0)
+    // descriptors differ only in their start-address field: build them once
     const uint64_t dQ[2] = {desc_sw128(sQ, 16, 1024), desc_sw128(sQ + C::kQTile, 16, 1024)};
-    uint64_t qoff = 0;   // start-address offset of the current unit's Q buffer
     const uint64_t dK0 = desc_sw128(sKV, 16, 1024);
     const uint64_t dV0 = desc_sw128(sKV, C::kRegionBytes, 1024);
     auto issue_S = [&](int x, int st) {
@@ -587,7 +535,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < H / 16; ++kk) {
         const uint64_t off = (uint64_t)(((kk / 4) * C::kRegionBytes + (kk % 4) * 32) >> 4);
-        if (leader) mma_f16_ss(tS[x], dQ[x] + qoff + off, dk + off, kIdQK, kk > 0);
+        if (leader) mma_f16_ss(tS[x], dQ[x] + off, dk + off, kIdQK, kk > 0);
       }
     };
     auto issue_PV = [&](int x, int st, bool acc) {
@@ -612,9 +560,8 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
       decode_unit(a, u, w);
       const int n = w.n_tiles;
       if (n == 0) continue;
-      if (!(ok = wait_all(q_prologue ? b_qready : b_qfull(it & 1), q_prologue ? (it & 1) : ((it >> 1) & 1)))) break;
+      if (!(ok = wait_all(q_prologue ? b_qready : b_qfull, it & 1))) break;
       tc_fence_after();
-      qoff = (uint64_t)(((it & 1) * C::kQBuf) >> 4);
       ++it;
       if (!(ok = wait_full(seq))) break;
       {
@@ -626,6 +573,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
         }
         if (!ok) break;
         ++ns;
+        if (n == 1) commit(b_qempty);   // the unit's last S MMAs have been issued
         commit(b_empty(st));
         ++seq;
       }
@@ -651,6 +599,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
           if (!ok) break;
           ++np;
           if (more) ++ns;
+          if (more && j + 2 == n) commit(b_qempty);
           commit(b_empty(vst));
           if (more) {
             commit(b_empty(kst));
@@ -671,6 +620,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
             }
             if (!ok) break;
             ++ns;
+            if (j + 2 == n) commit(b_qempty);
             commit(b_empty(kst));
           }
           const int vst = seq % C::kStages;
@@ -764,9 +714,9 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
       if (n_tiles > 0 && q_prologue) {
         // add the query segment of the projection bias to this row of Q (this thread's part
         // of the columns) in shared memory
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_qfull(it & 1), (it >> 1) & 1, abortp, a.wait_ns));
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_qfull, it & 1, abortp, a.wait_ns));
         if (ok) {
-          const uint32_t qRow = sQ + (it & 1) * C::kQBuf + x * C::kQTile + row * 128;
+          const uint32_t qRow = sQ + x * C::kQTile + row * 128;
           const T* qb = reinterpret_cast<const T*>(a.q_bias) + (int64_t)qh * H;
           const int swz = row & 7;
 #pragma unroll
@@ -791,9 +741,13 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
         mbar_arrive(b_qready);
         if (!ok) break;
       }
-      const int qbuf = it & 1;   // this unit's Q buffer (units with work)
       if (n_tiles > 0) ++it;
 
+      if constexpr (kStage) {
+        // the previous unit's y stores from this warp's mask region have read it
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
+      }
       float m_use = (kMode == kCapFixed) ? m_fixed : -INFINITY, l = 0.f;
       for (int j = 0; j < n_tiles && ok; ++j) {
         bool staged = false;     // warp-uniform: the mask tile comes through shared memory
@@ -1135,11 +1089,13 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
       const float inv = (denom > 0.f && m_use != -INFINITY) ? 1.f / denom : 0.f;
       T* yrow = reinterpret_cast<T*>(a.y) + (int64_t)b * a.y_sb + (int64_t)qh * a.y_sh + i * a.y_ss +
                 (H / kSplit) * hh;
-      // y: staged in this unit's Q buffer (row = TMEM lane, the Q tiles' 128-byte swizzle)
-      // for the TMA stores of warp 2; a unit with no admitted key writes its zero rows
-      // directly
+      // y through shared memory: the warp's 32 rows, 64 columns at a time, one TMA store each
+      // (rows past S are clipped by the tensor map); a unit with no admitted key writes its
+      // zero rows directly
       const bool write_y = !kStats || a.y != nullptr;
-      const uint32_t sYrow = sQ + qbuf * C::kQBuf + x * C::kQTile + row * 128;
+      const uint32_t sY = kStage ? sMask : sbase + C::kYOff + (uint32_t)(x * 4 + sub) * C::kYWarpBytes;
+      int yc1 = 0, yc2 = 0, yc3 = 0;
+      if (write_y && n_tiles > 0) perm_coords(a.y_ds, a.y_dn, a.y_db, mx0 + sub * 32, qh, b, yc1, yc2, yc3);
       constexpr bool stats = kStats && kSplit == 1;   // the backward's statistics pass
       const T* dyrow = stats ? reinterpret_cast<const T*>(a.dy) + (int64_t)b * a.dy_sb + (int64_t)qh * a.dy_sh +
                                    i * a.dy_ss
@@ -1167,6 +1123,11 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
         }
         if (n_tiles > 0) {
           if (write_y) {
+            if ((c & 1) == 0) {
+              // the warp's previous store has finished reading the staging buffer
+              if (lane == 0) bulk_wait_read<0>();
+              __syncwarp();
+            }
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               uint32_t wv[4];
@@ -1176,9 +1137,16 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
                 const float v1 = __uint_as_float(o[q * 8 + 2 * e + 1]) * inv;
                 wv[e] = kBF16 ? pack_bf16x2(v0, v1) : pack_f16x2(v0, v1);
               }
-              const int col = (H / kSplit) * hh + c * 32 + q * 8;   // first column of the piece
-              const uint32_t addr = sYrow + (col >> 6) * C::kRegionBytes + ((((col & 63) >> 3) ^ (row & 7)) << 4);
-              st_shared_v4(addr, wv[0], wv[1], wv[2], wv[3]);
+              const int c16 = (c & 1) * 4 + q;   // 16-byte piece of the row within the 64 columns
+              st_shared_v4(sY + lane * 128 + ((c16 ^ (lane & 7)) << 4), wv[0], wv[1], wv[2], wv[3]);
+            }
+            if ((c & 1) == 1) {
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_4d(&ty, sY, (c >> 1) * 64, yc1, yc2, yc3);
+                bulk_commit();
+              }
             }
           }
         } else if (valid && write_y) {
@@ -1200,14 +1168,12 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
         a.lse2_out[r_idx] = (denom > 0.f && m_use != -INFINITY) ? m_use + log2f(denom) : INFINITY;
         a.delta_out[r_idx] = delta;
       }
-      if (n_tiles > 0) {
-        // y is in the buffer, visible to the TMA stores
-        fence_proxy_async_smem();
-        mbar_arrive(b_ystaged(qbuf));
-      }
       // the epilogue's tensor-memory reads are complete before this thread's next P store,
       // which the MMA warp waits for before the next unit's first PV overwrites O
     }
+    // the warp's last stores have read shared memory before the CTA exits
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   // ---- teardown
@@ -1432,10 +1398,10 @@ cudaError_t launch_prefill_tc_stats(const Problem& p, sdpa_dtype dt, float* lse2
   if (!make_map(&tv, p.v, dt, p.B, p.Nkv, p.T, p.Hv, &vds, &vdn, &vdb)) return cudaErrorInvalidValue;
 
   if (vds != a.kv_ds || vdn != a.kv_dn || vdb != a.kv_db) return cudaErrorInvalidValue;   // k and v views differ in order
-  // y: one 64-column x 128-row box per store; a statistics pass without y never stores and
+  // y: one 64-column x 32-row box per store; a statistics pass without y never stores and
   // takes Q's map as a stand-in
   CUtensorMap ty = tq;
-  if (p.y.p && !make_map(&ty, p.y, dt, p.B, p.Nq, p.S, p.Hv, &a.y_ds, &a.y_dn, &a.y_db, 128))
+  if (p.y.p && !make_map(&ty, p.y, dt, p.B, p.Nq, p.S, p.Hv, &a.y_ds, &a.y_dn, &a.y_db, 32))
     return cudaErrorInvalidValue;
   // work units: two heads of a group over one row block when the group is even, else two
   // consecutive row blocks of one head
