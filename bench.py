@@ -6,6 +6,8 @@ JSON line on rank 0.  The other workloads are measured in the same run and repor
 "secondary" (decode in KV GB/s).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
+  python bench.py --profile-run --workload W [--batch B] [--rope] [--qk-mode M] [--iters K]
+  python bench.py --profile-run --rotary | --backward --workload 3 [--iters K]
 
 --impl reference times the double-precision CPU oracle (the only other program this
 repository has for the same computation) on bounded samples of the same workload.
@@ -80,8 +82,46 @@ def decode_bytes(case: Case) -> float:
     return float(past + new + present + qy)
 
 
+def decode_attended_bytes(case: Case) -> float:
+    """The secondary decode figure: bytes of the K/V-cache rows the step actually attends
+    (positions j < keylen[b] of every kv head), without the present copy."""
+    es = torch.tensor([], dtype=case.dtype).element_size()
+    T = case.T
+    if case.lens is not None and case.len_kind in ("keylen", "nonpad"):
+        keys = sum(min(int(n), T) for n in case.lens.tolist())
+    elif case.lens is not None and case.len_kind == "seqlens_k":
+        keys = sum(min(int(n) + 1, T) for n in case.lens.tolist())
+    else:
+        keys = case.B * T
+    return float(keys * case.Nkv * (case.H + case.Hv) * es)
+
+
 def is_decode(idx: int) -> bool:
     return idx == 4
+
+
+# NVIDIA's GB300 dense BF16/FP16 tensor rate (per GPU, without 2:4 sparsity), the nominal
+# figure the measured cuBLAS peak is compared with
+NOMINAL_BF16_TFLOPS = 2250.0
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (x86 /proc/cpuinfo, else lscpu, else the machine type)."""
+    try:
+        for ln in open("/proc/cpuinfo"):
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for ln in out.splitlines():
+            if ln.lower().startswith("model name"):
+                return ln.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    import platform
+    return platform.machine()
 
 
 # ------------------------------------------------------------------------------ helpers
@@ -206,10 +246,13 @@ HOST_LEAD_CYCLES = 4_000_000       # ~2 ms of GPU sleep ahead of the timed steps
 
 def time_device(fn, steps, warmup, flush_buf, barrier):
     """CUDA-event times of `steps` calls of fn on the current stream (L2 flushed before each
-    when flush_buf is given, outside the events).  A short device-side sleep is queued ahead
-    of the first timed step, so that the host has enqueued the first steps before the GPU
-    reaches them: an event pair then brackets device work only, never the GPU idling while
-    the host prepares a call."""
+    when flush_buf is given, outside the events).  The flush buffer is written once before the
+    warm-ups (its first write maps fresh pages and slows the kernel that follows it), and a
+    short device-side sleep is queued ahead of the first timed step, so that the host has
+    enqueued the first steps before the GPU reaches them: an event pair then brackets device
+    work only, never the GPU idling while the host prepares a call."""
+    if flush_buf is not None:
+        flush_buf.fill_(0)              # first touch of the flush buffer outside the timed region
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
@@ -425,10 +468,13 @@ def roofline(idx: int, case: Case, res: dict, hbm, tfl, tfl_src):
         achieved = decode_bytes(case) / (ms * 1e-3) / 1e9
         return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                 "frac": achieved / hbm, "peak_source": f"{tfl_src} copy bandwidth",
-                "traffic": ncu_traffic(res["kernel"])}
+                "traffic": ncu_traffic(res["kernel"]),
+                "attended_kv_GBps": decode_attended_bytes(case) / (ms * 1e-3) / 1e9}
     achieved = prefill_flops(case) / (ms * 1e-3) / 1e12
     return {"bound": "tensor", "achieved": achieved, "peak": tfl, "unit": "TFLOP/s",
             "frac": achieved / tfl, "peak_source": f"{tfl_src} bf16 dense burst",
+            "frac_of_nominal": achieved / NOMINAL_BF16_TFLOPS,
+            "nominal_peak": f"{NOMINAL_BF16_TFLOPS:.0f} TFLOP/s dense bf16 (NVIDIA GB300 figure)",
             "traffic": ncu_traffic(res["kernel"])}
 
 
@@ -471,7 +517,7 @@ class OracleSampler:
         else:
             work = float(self.counts[rows[:, 0], rows[:, 2]].sum()) * 2.0 * (c.H + c.Hv)
             value, unit = work / secs / 1e12, "TFLOP/s"
-        return {"value": value, "unit": unit, "cores": threads, "kind": "oracle",
+        return {"value": value, "unit": unit, "cores": threads, "cpu_model": cpu_model(), "kind": "oracle",
                 "sample": f"{n} of {c.B * c.Nq * c.S} query rows of {c.name}, {secs:.2f} s on {threads} threads",
                 "seconds": secs}
 
@@ -522,7 +568,18 @@ def main():
                     help="measure only the backward on the GQA workload (profiling captures)")
     ap.add_argument("--ref-seconds", type=float, default=150.0,
                     help="total CPU time budget of the reference (oracle) arm")
+    # profiler captures: run one case --iters times through the C ABI, untimed
+    ap.add_argument("--profile-run", action="store_true",
+                    help="run --workload (or --rotary / --backward) --iters times for a profiler capture, no timing")
+    ap.add_argument("--iters", type=int, default=3)
+    ap.add_argument("--rope", action="store_true", help="--profile-run: rotate Q and the new K rows first")
+    ap.add_argument("--qk-mode", type=int, default=None, help="--profile-run: also write the qk output at this stage")
+    ap.add_argument("--rotary", action="store_true", help="--profile-run: the standalone rotary shape")
+    ap.add_argument("--backward", action="store_true", help="--profile-run: the backward of --workload")
     a = ap.parse_args()
+    if a.profile_run:
+        profile_run(a)
+        return
     warmup = max(3, a.warmup)
     idx = a.workload
 
@@ -588,6 +645,7 @@ def main():
         "config": config_of(idx, case, res),
         "kernel": res["kernel"],
         "ms_p10_p90": [float(np.percentile(res["ms"], 10)), float(np.percentile(res["ms"], 90))],
+        "ms_median": float(np.median(res["ms"])),
         "clocks": res["clocks"],
         "gpu_launches": res["launches"],
         "e2e": ({"value": e2e_value * ws, "unit": unit, "h2d_bytes_per_step": res["h2d"],
@@ -602,43 +660,44 @@ def main():
         line["cpu_baseline"] = {k: v for k, v in oracle_sample(idx, a.cpu_seconds, case).items()
                                 if k != "seconds"}
     if not a.no_secondary:
-        sec = []
+        # the other workloads and the NEXT rows, compact and last on the line, so that a
+        # reader keeping only the line's tail still sees them:
+        #   secondary [workload, value, unit, ms per step, roofline fraction, kernel]
+        sec, sec_ms = [], {}
         for j in sorted(WORKLOADS):
             if j == idx:
                 continue
             r = measure_native(j, max(5, min(a.steps // 2, 200)), warmup, barrier, with_e2e=False)
             m = statistics.mean(r["ms"])
             v, u = metric_of(j, r["case"], m)
-            sec.append({"workload": r["case"].name, "value": v, "unit": u, "ms_per_step": m,
-                        "kernel": r["kernel"], "gpu_launches": r["launches"],
-                        "roofline": roofline(j, r["case"], r, hbm, tfl, src) if j != 1 else None,
-                        "l2_flush": r["l2_flush"], "clocks": r["clocks"]})
+            rf = roofline(j, r["case"], r, hbm, tfl, src) if j != 1 else None
+            entry = [r["case"].name, round(v, 2), u, round(m, 5), None if rf is None else round(rf["frac"], 4), r["kernel"]]
+            if rf is not None and "attended_kv_GBps" in rf:
+                entry.append({"attended_kv_GBps": round(rf["attended_kv_GBps"], 1)})
+            sec.append(entry)
+            sec_ms[j] = m
             del r
             torch.cuda.empty_cache()
-        line["secondary"] = sec
-        # the rotary embedding: standalone, and as the prologue of the GQA prefill and of
-        # the decode step (overhead against the same workload without it)
-        nxt = [measure_rotary(max(20, min(a.steps, 500)), warmup, barrier, hbm)]
+        # rotary [workload, value, unit, ms per step, overhead against the same workload
+        # without the rotation (ms)]: standalone, and as the prologue of the GQA prefill and
+        # of the decode step
+        rot = measure_rotary(max(20, min(a.steps, 500)), warmup, barrier, hbm)
+        nxt = [[rot["workload"], round(rot["value"], 1), rot["unit"], round(rot["ms_per_step"], 5), None]]
         for j in (2, 4):
             r = measure_native(j, max(5, min(a.steps // 2, 200)), warmup, barrier, with_e2e=False, rope=True)
             m = statistics.mean(r["ms"])
             v, u = metric_of(j, r["case"], m)
-            base_ms = ms if j == idx else next((x["ms_per_step"] for x in sec if x["workload"] ==
-                                               WORKLOADS[j]), None)
-            nxt.append({"workload": r["case"].name, "value": v, "unit": u, "ms_per_step": m,
-                        "kernel": r["kernel"], "gpu_launches": r["launches"],
-                        "rope_overhead_ms": None if base_ms is None else m - base_ms,
-                        "l2_flush": r["l2_flush"], "clocks": r["clocks"]})
+            base_ms = ms if j == idx else sec_ms.get(j)
+            nxt.append([r["case"].name, round(v, 2), u, round(m, 5), None if base_ms is None else round(m - base_ms, 5)])
             del r
             torch.cuda.empty_cache()
-        line["rotary"] = nxt
-        # the backward (GroupQueryAttention gradient graph) on the windowed GQA workload
-        line["backward"] = [measure_backward(3, max(5, min(a.steps // 2, 100)), warmup, barrier, tfl, src)]
+        # backward [workload, value, unit, ms per step, roofline fraction, launches per step]
+        bw = measure_backward(3, max(5, min(a.steps // 2, 100)), warmup, barrier, tfl, src)
         torch.cuda.empty_cache()
-        # the auxiliary qk output (qk_matmul_output_mode 0 and 3) on the GQA prefill: the
-        # output write is the added work; GB/s counts its bytes over the added time
+        # qk output [workload, ms per step, added ms, GB/s of qk output over the added time,
+        # fraction of HBM]: qk_matmul_output_mode 0 and 3 on the GQA prefill
+        qkl = []
         if idx == 2:
-            qkl = []
             for mode in (0, 3):
                 r = measure_native(2, max(5, min(a.steps // 2, 200)), warmup, barrier, with_e2e=False, qk_mode=mode)
                 m = statistics.mean(r["ms"])
@@ -646,15 +705,56 @@ def main():
                 out_bytes = c.B * c.Nq * c.S * c.T * 4
                 extra_ms = m - ms
                 gbs = out_bytes / (extra_ms * 1e-3) / 1e9 if extra_ms > 0 else None
-                qkl.append({"workload": c.name + f"_qk_mode{mode}", "ms_per_step": m, "qk_extra_ms": extra_ms,
-                            "qk_out_bytes": out_bytes, "qk_GBps_over_extra_time": gbs,
-                            "frac_of_hbm": None if gbs is None else gbs / hbm,
-                            "traffic": ncu_traffic("qk_tc_bf16_h128") if mode == 0 else None,
-                            "kernel": r["kernel"], "gpu_launches": r["launches"]})
+                qkl.append([c.name + f"_qk_mode{mode}", round(m, 5), round(extra_ms, 5),
+                            None if gbs is None else round(gbs, 1), None if gbs is None else round(gbs / hbm, 4)])
                 del r
                 torch.cuda.empty_cache()
+        line["rotary"] = nxt
+        line["backward"] = [[bw["workload"], round(bw["value"], 2), bw["unit"], round(bw["ms_per_step"], 5),
+                             round(bw["roofline"]["frac"], 4), bw["launches_per_step"]]]
+        if qkl:
             line["qk_output"] = qkl
+        line["secondary"] = sec
     print(json.dumps(line))
+
+
+def profile_run(a):
+    """Runs one case a.iters times through the C ABI (for ncu captures; nothing is timed) and
+    prints the kernel name and the device status word."""
+    from scaled_dot_product_gb300 import build as _b, sdpa
+    from scaled_dot_product_gb300.workloads import as4d, draw_dy, make_rotary_inputs, rope_caches
+    _b.build()
+    torch.cuda.set_device(0)
+    if a.rotary:
+        sh = ROTARY_SHAPE
+        ri = make_rotary_inputs(dtype=torch.bfloat16, layout="bsnh", cache="ids", max_pos=2 * sh["S"], seed=7,
+                                **sh).to("cuda")
+        y = torch.empty_like(ri.x)
+        for _ in range(a.iters):
+            sdpa.sdpa_rotary(ri.x, ri.cos, ri.sin, ri.position_ids, num_heads=sh["N"], y=y)
+    elif a.backward:
+        case_cpu = workload(a.workload, batch=a.batch)
+        case = case_cpu.to("cuda")
+        q, k, v = case.views()
+        dy = as4d(draw_dy(case_cpu, seed=3000 + a.workload).to("cuda"), case.q_layout, case.Nq)
+        for _ in range(a.iters):
+            sdpa.sdpa_attn_bwd(q, k, v, dy, **sdpa.case_kwargs(case))
+    else:
+        case = workload(a.workload, batch=a.batch)
+        if a.rope:
+            case.rotary_cos, case.rotary_sin = rope_caches(case.T, case.H // 2, case.dtype)
+        case = case.to("cuda")
+        op = "decode" if is_decode(a.workload) else "fwd"
+        ws = sdpa.case_workspace(case, op)
+        outs = sdpa.case_outputs(case)
+        extra = {}
+        if a.qk_mode is not None:
+            extra = dict(qk_out=torch.empty(case.B, case.Nq, case.S, case.T, dtype=torch.float32, device="cuda"),
+                         qk_mode=a.qk_mode)
+        for _ in range(a.iters):
+            sdpa.run_case(case, op, outputs=outs, workspace=ws, **extra)
+    torch.cuda.synchronize()
+    print("kernel", sdpa.sdpa_last_kernel_name(), "status", sdpa.sdpa_query_status())
 
 
 def metric_name(idx: int) -> str:
