@@ -202,7 +202,9 @@ SDPA_API int sdpa_attn_decode(const sdpa_params* p, void* workspace, size_t work
  *    must fit in 8 MiB, else SDPA_ERR_WORKSPACE is returned and nothing is launched.
  *    E.g. 2048 rows, T = 4096, Hv = 128 need about 4.3 MiB.
  *  - The first call on each device looks up the array's device address with that device
- *    current; make that first call before any stream capture on the device.
+ *    current, and so does the first call after the device's context has changed (e.g.
+ *    after cudaDeviceReset, which may load the library's device code elsewhere); make
+ *    those calls before any stream capture on the device.
  *  - Calls no cudaMalloc, cudaFree or other allocating routine.
  *  - Every call on a device shares the one array, which keeps the last call's contents
  *    (nothing in it needs to start at zero: each call writes every slot it reads).  Calls

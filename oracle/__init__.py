@@ -248,6 +248,29 @@ def attention(pr: Problem, nthreads: int = 0) -> np.ndarray:
     return out.reshape(B, Nq, S, Hv)
 
 
+def mha_projection_bias(bias: Optional[torch.Tensor], num_heads: int, head_size: int, v_head_size: int,
+                        kv_rank: int):
+    """The projection-bias segments MultiHeadAttention applies ("Custom operators", section
+    Microsoft MultiHeadAttention): the bias input is one vector of N*H + N*H + N*Hv values,
+    the query, key and value segments in that order (the order of its size formula).  The
+    query segment is always added to the query; the key and value segments are added only to
+    rank-3 (packed, not yet split into heads) key and value inputs: for rank-4 key/value
+    (cross-attention with pre-projected heads) only the query segment is applied.
+
+    Returns (q_bias, k_bias, v_bias) as slices of `bias`, None where a segment is not applied."""
+    if bias is None:
+        return None, None, None
+    nh, nhv = num_heads * head_size, num_heads * v_head_size
+    if bias.dim() != 1 or bias.numel() != 2 * nh + nhv:
+        raise ValueError(f"projection bias must be ({2 * nh + nhv},), got {tuple(bias.shape)}")
+    if kv_rank not in (3, 4):
+        raise ValueError("key/value rank must be 3 or 4")
+    q_seg = bias[:nh]
+    if kv_rank == 4:
+        return q_seg, None, None
+    return q_seg, bias[nh:2 * nh], bias[2 * nh:]
+
+
 def present(past: Optional[torch.Tensor], cur: torch.Tensor, bias: Optional[torch.Tensor] = None
             ) -> torch.Tensor:
     """present = concat(past, cur [+ bias]) along the sequence axis, (B, N, P+L, D) contiguous."""

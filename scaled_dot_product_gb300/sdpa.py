@@ -269,6 +269,53 @@ def sdpa_attn_fwd(q, k, v, *, y=None, workspace=None, stream=None, **kw) -> torc
     return _run(lib().sdpa_attn_fwd, SDPA_OP_FWD, q, k, v, y, workspace, stream, kw)
 
 
+def mha_bias_segments(projection_bias: Optional[torch.Tensor], num_heads: int, H: int, Hv: int,
+                      kv_rank: int):
+    """(q_bias, k_bias, v_bias) for the C ABI from MultiHeadAttention's single projection-bias
+    input ("Custom operators", Microsoft MultiHeadAttention): [query N*H | key N*H | value N*Hv];
+    rank-4 key/value take no key/value segment (only the query segment applies).  Slices of
+    the input: pointer offsets, no arithmetic."""
+    if projection_bias is None:
+        return None, None, None
+    nq, nv = num_heads * H, num_heads * Hv
+    if projection_bias.dim() != 1 or projection_bias.numel() != 2 * nq + nv:
+        raise ValueError(f"projection bias of {2 * nq + nv} values expected, got {tuple(projection_bias.shape)}")
+    segments = (projection_bias[:nq], projection_bias[nq:2 * nq], projection_bias[2 * nq:])
+    if kv_rank == 4:
+        return segments[0], None, None
+    if kv_rank != 3:
+        raise ValueError("key/value must be rank 3 or rank 4")
+    return segments
+
+
+def _heads4(t: torch.Tensor, num_heads: int) -> torch.Tensor:
+    """(B, N, S, D) view of a rank-3 (B, S, N*D) tensor; rank-4 tensors pass through."""
+    if t.dim() == 4:
+        return t
+    B, S, ND = t.shape
+    return t.view(B, S, num_heads, ND // num_heads).permute(0, 2, 1, 3)
+
+
+def sdpa_mha_fwd(query, key, value, *, num_heads: int, projection_bias=None, y=None, workspace=None,
+                 stream=None, **kw) -> torch.Tensor:
+    """MultiHeadAttention forward over the operator's tensors: query (B, S, N*H); key and value
+    rank-3 (B, L, N*H) / (B, L, N*Hv) or rank-4 (B, N, L, H) / (B, N, L, Hv); projection_bias
+    the operator's single (2*N*H + N*Hv,) input, of which rank-4 key/value take only the query
+    segment.  Returns y (B, S, N*Hv).  Other keywords as sdpa_attn_fwd (masks, lengths,
+    past/present, scale, causal / unidirectional, mask_filter_value)."""
+    if key.dim() != value.dim() or key.dim() not in (3, 4):
+        raise ValueError("key and value must both be rank 3 or both rank 4")
+    q4, k4, v4 = _heads4(query, num_heads), _heads4(key, num_heads), _heads4(value, num_heads)
+    B, N, S, H = q4.shape
+    Hv = v4.shape[3]
+    q_bias, k_bias, v_bias = mha_bias_segments(projection_bias, num_heads, H, Hv, key.dim())
+    if y is None:
+        y = torch.empty(B, S, N * Hv, dtype=query.dtype, device=query.device)
+    sdpa_attn_fwd(q4, k4, v4, y=_heads4(y, num_heads), workspace=workspace, stream=stream,
+                  q_bias=q_bias, k_bias=k_bias, v_bias=v_bias, **kw)
+    return y
+
+
 def sdpa_attn_decode(q, k, v, *, y=None, workspace=None, stream=None, **kw) -> torch.Tensor:
     """Split-KV decode (S <= 16), same arguments as sdpa_attn_fwd."""
     return _run(lib().sdpa_attn_decode, SDPA_OP_DECODE, q, k, v, y, workspace, stream, kw)
@@ -276,10 +323,12 @@ def sdpa_attn_decode(q, k, v, *, y=None, workspace=None, stream=None, **kw) -> t
 
 def sdpa_attn_decode_static(q, k, v, *, y=None, stream=None, **kw) -> torch.Tensor:
     """Decode without a workspace (the library's built-in device scratch), for callers
-    that cannot allocate device memory; same arguments as sdpa_attn_decode otherwise.
-    Calls that overlap on the GPU share that scratch and race: keep them on one stream."""
+    that cannot allocate device memory; same arguments as sdpa_attn_decode otherwise, except
+    that the caller passes the output y (B, Nq, S, Hv): like the C call, this binding
+    allocates nothing.  Calls that overlap on the GPU share that scratch and race: keep them
+    on one stream."""
     if y is None:
-        y = torch.empty(q.shape[0], q.shape[1], q.shape[2], v.shape[3], dtype=q.dtype, device=q.device)
+        raise ValueError("sdpa_attn_decode_static allocates nothing: pass the output y")
     params, keep = make_params(q, k, v, y=y, **kw)
     _check(lib().sdpa_attn_decode_static(ctypes.byref(params), _stream(stream)))
     return y

@@ -422,6 +422,34 @@ def test_projection_bias_length_matches_the_contract():
         assert 2 * c["N"] * c["H"] + c["N"] * c["Hv"] == c["length"]
 
 
+def test_mha_projection_bias_rank4_cross_attention_takes_only_the_query_segment():
+    """MultiHeadAttention ("Custom operators"): for rank-4 (cross-attention) key/value only the
+    query segment of the projection bias is applied, so changing the key and value segments
+    leaves Y unchanged; for rank-3 (packed) key/value every segment applies, in the order
+    [query | key | value]."""
+    B, N, S, T, H, Hv = 2, 3, 4, 9, 8, 4
+    q, k, v = rnd(B, N, S, H, seed=131), rnd(B, N, T, H, seed=132), rnd(B, N, T, Hv, seed=133)
+    bias = rnd(2 * N * H + N * Hv, seed=134)
+    moved = bias.clone()
+    moved[N * H:] += rnd(N * H + N * Hv, seed=135)           # other key / value segments
+    seg4 = oracle.mha_projection_bias(bias, N, H, Hv, kv_rank=4)
+    assert seg4[1] is None and seg4[2] is None
+    y4 = run(q, k, v, q_bias=seg4[0])
+    np.testing.assert_array_equal(y4, run(q, k, v, q_bias=oracle.mha_projection_bias(moved, N, H, Hv, 4)[0]))
+    # the query segment does matter, and it is the first N*H values
+    np.testing.assert_allclose(y4, sdpa(q + bias[:N * H].view(1, N, 1, H), k, v), atol=1e-12)
+    # rank-3 key/value: all three segments, and moving the key / value segments changes Y
+    qb, kb, vb = oracle.mha_projection_bias(bias, N, H, Hv, kv_rank=3)
+    y3 = run(q, k, v, q_bias=qb, k_bias=kb, v_bias=vb)
+    want = sdpa(q + bias[:N * H].view(1, N, 1, H), k + bias[N * H:2 * N * H].view(1, N, 1, H),
+                v + bias[2 * N * H:].view(1, N, 1, Hv))
+    np.testing.assert_allclose(y3, want, atol=1e-12)
+    qm, km, vm = oracle.mha_projection_bias(moved, N, H, Hv, kv_rank=3)
+    assert np.abs(run(q, k, v, q_bias=qm, k_bias=km, v_bias=vm) - y3).max() > 1e-3
+    with pytest.raises(ValueError):
+        oracle.mha_projection_bias(bias[:-1], N, H, Hv, 3)
+
+
 def test_oracle_rejects_window_without_causal_and_bad_groups():
     q, k, v = rnd(1, 3, 2, 4, seed=75), rnd(1, 2, 2, 4, seed=76), rnd(1, 2, 2, 4, seed=77)
     with pytest.raises(ValueError):

@@ -219,23 +219,54 @@ def test_kv_concat_bit_exact_with_and_without_bias():
             assert torch.equal(pres.cpu().view(iv), want.view(iv)), (dtype, b is not None)
 
 
-# ----------------------------------------------------------------- full-size workloads, sampled rows
+# ----------------------------------------------------------------- MultiHeadAttention projection bias
 
-def _sample_rows(case: Case, n: int, seed: int) -> np.ndarray:
-    rng = np.random.default_rng(seed)
-    rows = np.stack([rng.integers(0, case.B, n), rng.integers(0, case.Nq, n),
-                     rng.integers(0, case.S, n)], -1)
-    edges = np.array([[0, 0, 0], [case.B - 1, case.Nq - 1, case.S - 1],
-                      [case.B - 1, 0, case.S - 1], [0, case.Nq - 1, min(case.S - 1, 127)],
-                      [0, 0, min(case.S - 1, 128)]])
-    return np.concatenate([rows, edges]).astype(np.int64)
+def test_mha_projection_bias_rank4_cross_attention():
+    """The operator's single projection-bias input through sdpa_mha_fwd: with rank-4 key/value
+    (the cross-attention workload) only the query segment applies, so non-zero key and value
+    segments leave y bit-identical and equal to the oracle's; with rank-3 key/value every
+    segment applies."""
+    c = workload(5, small=True)
+    N, H, Hv = c.Nq, c.H, c.Hv
+    bias = c.proj_bias
+    assert bias is not None and bias.numel() == 2 * N * H + N * Hv
+    assert bias[N * H:].abs().max() > 0                       # the key / value segments are not zero
+    zeroed = bias.clone()
+    zeroed[N * H:] = 0
+    d = c.to("cuda")
+    am = d.add_mask
+    y = sdpa.sdpa_mha_fwd(d.q, d.k, d.v, num_heads=N, projection_bias=bias.cuda(), add_mask=am,
+                          mask_filter_value=c.mask_filter_value)
+    y0 = sdpa.sdpa_mha_fwd(d.q, d.k, d.v, num_heads=N, projection_bias=zeroed.cuda(), add_mask=am,
+                           mask_filter_value=c.mask_filter_value)
+    torch.cuda.synchronize()
+    assert sdpa.sdpa_query_status() == sdpa.SDPA_OK
+    assert torch.equal(y.view(torch.int16), y0.view(torch.int16))
+    pr = problem(c)
+    pr.q_bias, pr.k_bias, pr.v_bias = oracle.mha_projection_bias(bias, N, H, Hv, kv_rank=4)
+    want = oracle.attention(pr)
+    err = np.abs(y_as_bnsh(c, y) - want).max()
+    assert err <= TOL[c.dtype], err
+    # the same problem with packed rank-3 key/value: the key and value segments apply
+    k3 = d.k.permute(0, 2, 1, 3).reshape(c.B, c.L, N * H).contiguous()
+    v3 = d.v.permute(0, 2, 1, 3).reshape(c.B, c.L, N * Hv).contiguous()
+    y3 = sdpa.sdpa_mha_fwd(d.q, k3, v3, num_heads=N, projection_bias=bias.cuda(), add_mask=am,
+                           mask_filter_value=c.mask_filter_value)
+    torch.cuda.synchronize()
+    pr.q_bias, pr.k_bias, pr.v_bias = oracle.mha_projection_bias(bias, N, H, Hv, kv_rank=3)
+    err3 = np.abs(y_as_bnsh(c, y3) - oracle.attention(pr)).max()
+    assert err3 <= TOL[c.dtype], err3
 
+
+# ----------------------------------------------------------------- full-size workloads, every row
 
 @pytest.mark.slow
 @pytest.mark.parametrize("idx,op", [(2, "fwd"), (3, "fwd"), (4, "decode"), (4, "fwd"), (5, "fwd"), (6, "fwd")])
-def test_workload_full_size_sampled(idx, op):
-    case = workload(idx)
-    run_and_compare(case, op, rows=_sample_rows(case, 96, 100 + idx))
+def test_workload_full_size(idx, op):
+    """Every output element of the full-size workloads (the configuration bench.py times)
+    against the oracle, and present bit-exact; the oracle takes seconds per workload on the
+    host's cores."""
+    run_and_compare(workload(idx), op)
 
 
 # ----------------------------------------------------------------- bf16 softcap, fixed maximum
