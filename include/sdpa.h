@@ -68,6 +68,8 @@ typedef struct CUstream_st* sdpa_stream_t;   /* same type as cudaStream_t */
 #define SDPA_ERR_CUDA         8   /* a CUDA runtime/driver call failed                       */
 #define SDPA_ERR_TIMEOUT      9   /* a bounded device-side wait expired (via query_status)   */
 #define SDPA_ERR_NULL        10   /* a required pointer is NULL                              */
+#define SDPA_ERR_BOUNDS      11   /* bounds-checking build only: an index check failed and   */
+                                  /* the access was skipped (via sdpa_query_status)          */
 
 typedef enum { SDPA_F32 = 0, SDPA_F16 = 1, SDPA_BF16 = 2 } sdpa_dtype;
 

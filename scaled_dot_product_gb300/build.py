@@ -37,16 +37,23 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, extra_flags=None) -> str:
+# The bounds-checking debug build: every guarded index is range-checked in the kernels; a
+# failed check records its site (sdpa_query_status: SDPA_ERR_BOUNDS) and skips the access.
+LIB_BOUNDS = os.path.join(PKG, "libsdpa_bounds.so")
+
+
+def build(verbose: bool = False, extra_flags=None, bounds_check: bool = False) -> str:
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    build_dir = BUILD + ("_bounds" if bounds_check else "")
+    lib_path = LIB_BOUNDS if bounds_check else LIB
+    os.makedirs(build_dir, exist_ok=True)
     sources = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     headers = glob.glob(os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(CSRC, "*.cuh")) + \
         glob.glob(os.path.join(INCLUDE, "*.h"))
-    flags = FLAGS + list(extra_flags or [])
+    flags = FLAGS + list(extra_flags or []) + (["-DSDPA_BOUNDS_CHECK"] if bounds_check else [])
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         if _stale(obj, [src] + headers + [__file__]):
             cmd = [nvcc] + ARCH + flags + ["-c", src, "-o", obj]
             if verbose:
@@ -60,15 +67,15 @@ def build(verbose: bool = False, extra_flags=None) -> str:
 
     with ThreadPoolExecutor(max_workers=max(1, min(len(sources), os.cpu_count() or 4))) as ex:
         objs = list(ex.map(compile_one, sources))
-    if _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if _stale(lib_path, objs):
+        tmp = lib_path + f".tmp{os.getpid()}"
         cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + objs + ["-lcudart"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(verbose="-v" in sys.argv))
+    print(build(verbose="-v" in sys.argv, bounds_check="--bounds-check" in sys.argv))

@@ -699,6 +699,14 @@ int sdpa_query_status(sdpa_stream_t stream) {
   if (e != cudaSuccess) return cuda_fail(e, "status read");
   if (!status) status = qk_status;
   if (!status) status = bwd_status;
+  // the bounds-checking build: the first failing index check of each kernel family
+  int site = 0;
+  for (auto take : {take_bounds_prefill, take_bounds_decode, take_bounds_concat, take_bounds_simt}) {
+    int v = 0;
+    if ((e = take(&v)) != cudaSuccess) return cuda_fail(e, "bounds status read");
+    if (!site) site = v;
+  }
+  if (site) return fail(SDPA_ERR_BOUNDS, "an index check failed at site %d; the access was skipped", site);
   if (status) return fail(SDPA_ERR_TIMEOUT, "a bounded device wait expired (code %d)", status);
   if (rot_status) return fail(SDPA_ERR_INVALID, "a rotary position fell outside its cos/sin cache");
   return SDPA_OK;

@@ -143,4 +143,41 @@ __device__ __forceinline__ float apply_rules(const Rules& r, const RowCtx& c, fl
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// ---------------------------------------------------------------------------------------
+// Bounds-checking debug build (compiled with -DSDPA_BOUNDS_CHECK)
+// ---------------------------------------------------------------------------------------
+// SDPA_IN_BOUNDS(cond, site) guards an index before the access it feeds: in the debug build a
+// false condition records `site` (the first failing check wins) in the translation unit's
+// status word and yields false, so the caller skips the access instead of faulting; in the
+// normal build it is `true` and costs nothing.  Each kernel translation unit defines its
+// reader with SDPA_DEFINE_BOUNDS_TAKE(name); sdpa_query_status reports a recorded site as
+// SDPA_ERR_BOUNDS.
+#ifdef SDPA_BOUNDS_CHECK
+static __device__ int g_bounds_site;   // one per translation unit
+__device__ __forceinline__ bool bounds_ok(bool cond, int site) {
+  if (!cond) atomicCAS(&g_bounds_site, 0, site);
+  return cond;
+}
+#define SDPA_IN_BOUNDS(cond, site) (::sdpa::bounds_ok((cond), (site)))
+#define SDPA_DEFINE_BOUNDS_TAKE(name)                                          \
+  cudaError_t name(int* site) {                                                \
+    int v = 0;                                                                 \
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_bounds_site, sizeof v);         \
+    if (e != cudaSuccess) return e;                                            \
+    *site = v;                                                                 \
+    if (v) {                                                                   \
+      const int zero = 0;                                                      \
+      e = cudaMemcpyToSymbol(g_bounds_site, &zero, sizeof zero);               \
+    }                                                                          \
+    return e;                                                                  \
+  }
+#else
+#define SDPA_IN_BOUNDS(cond, site) true
+#define SDPA_DEFINE_BOUNDS_TAKE(name) \
+  cudaError_t name(int* site) {       \
+    *site = 0;                        \
+    return cudaSuccess;               \
+  }
+#endif
+
 }  // namespace sdpa

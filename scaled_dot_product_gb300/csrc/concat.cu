@@ -36,6 +36,7 @@ __global__ void __launch_bounds__(256) kv_concat_kernel(View past, View cur, con
       src = reinterpret_cast<const T*>(cur.p) + cur.off(b, n, t - P);
       add = kBias;
     }
+    if (!SDPA_IN_BOUNDS(t < T_total && b < B && c < chunks_per_row, 301)) continue;
     uint4 u = __ldg(reinterpret_cast<const uint4*>(src) + c);
     if (kBias && add) {
       T* e = reinterpret_cast<T*>(&u);
@@ -77,5 +78,7 @@ cudaError_t launch_kv_concat(sdpa_dtype dt, int B, int N, int P, int L, int D, c
     default: return launch_t<__nv_bfloat16>(B, N, P, L, D, past, cur, bias, present, st);
   }
 }
+
+SDPA_DEFINE_BOUNDS_TAKE(take_bounds_concat)
 
 }  // namespace sdpa

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const Problem p,
       jj[u] = base + grp + (int64_t)u * KPI;
       kvec[u] = make_uint4(0u, 0u, 0u, 0u);
       vvec[u] = make_uint4(0u, 0u, 0u, 0u);
-      if (jj[u] < j_end) {
+      if (jj[u] < j_end && SDPA_IN_BOUNDS(jj[u] >= 0 && jj[u] < p.T && t * V < H, 201)) {
         kvec[u] = __ldg(row_vec<T>(p, false, b, kh, jj[u]) + t);
         vvec[u] = __ldg(row_vec<T>(p, true, b, kh, jj[u]) + t);
       }
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const Problem p,
         if (kb) add_bias_round<T>(kvec[u], kf, kb + kh * H + t * V);
         if (vb) add_bias_round<T>(vvec[u], vf[u], vb + kh * H + t * V);
       }
-      if (valid && write_present) {
+      if (valid && write_present && SDPA_IN_BOUNDS(jj[u] < p.T && kh < p.Nkv, 202)) {
         T* pk = reinterpret_cast<T*>(const_cast<void*>(p.present_k.p)) + p.present_k.off(b, kh, jj[u]);
         T* pv = reinterpret_cast<T*>(const_cast<void*>(p.present_v.p)) + p.present_v.off(b, kh, jj[u]);
         __stcs(reinterpret_cast<uint4*>(pk) + t, kvec[u]);
@@ -181,6 +181,7 @@ __global__ void __launch_bounds__(kThreads) decode_split_kernel(const Problem p,
     const int rr = r0 + r;
     const int h = kh * p.group + rr / p.S, i = rr % p.S;
     const int64_t slot = (((int64_t)b * p.Nq + h) * p.S + i) * nsplit + split;
+    if (!SDPA_IN_BOUNDS(h < p.Nq && i < p.S && split < nsplit, 203)) continue;
     ws_o[slot * H + d] = O;
     if (d == 0) { ws_ml[slot * 2] = M; ws_ml[slot * 2 + 1] = Ls; }
   }
@@ -304,5 +305,7 @@ cudaError_t launch_decode(const Problem& p, sdpa_dtype dt, const DecodePlan& pla
     default: return launch_t<__nv_bfloat16>(p, plan, ws, st);
   }
 }
+
+SDPA_DEFINE_BOUNDS_TAKE(take_bounds_decode)
 
 }  // namespace sdpa

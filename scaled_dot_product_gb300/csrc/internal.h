@@ -68,6 +68,13 @@ cudaError_t launch_bwd_tc(const Problem& p, sdpa_dtype dt, const View& dy, const
                           const View& dv, float* lse2, float* delta, cudaStream_t st, const char** name);
 cudaError_t take_bwd_status(int* status);
 
+// Bounds-checking debug build: the first failing index check of each translation unit
+// (its site code; 0 when none), read and cleared.  Always 0 in the normal build.
+cudaError_t take_bounds_prefill(int* site);
+cudaError_t take_bounds_decode(int* site);
+cudaError_t take_bounds_concat(int* site);
+cudaError_t take_bounds_simt(int* site);
+
 // Decode with the partials in the library's own device array (no workspace).
 size_t decode_static_scratch_bytes();
 cudaError_t launch_decode_static(const Problem& p, sdpa_dtype dt, const DecodePlan& plan, cudaStream_t st);

@@ -3,18 +3,22 @@
 // and the masking rules of onnx-light class Attention / MultiHeadAttention /
 // GroupQueryAttention applied per element in registers.
 //
-// One CTA owns two 128-row query tiles (A, B) of one (batch, query head) and streams the
-// key/value tiles of its kv head through a shared-memory ring:
+// Persistent: one CTA per SM walks a share of the work units (heavy first).  A unit is two
+// 128-row query tiles that stream the same key/value tiles: two query heads of one GQA group
+// over one row block, or two consecutive row blocks of one head.
 //
-//   warp 0      TMA producer: Q tiles once, then K_0, V_0, K_1, V_1, ... into the ring
-//   warp 1      MMA issuer (one thread): S_X = Q_X K_j^T into TMEM, O_X += P_X V_j
-//   warps 4-7   softmax for tile A: each thread owns one query row (TMEM lane = row)
-//   warps 8-11  softmax for tile B
+//   warp 0      TMA producer: the unit's Q tiles (once the previous unit's last S MMAs have
+//               read the buffer), then K_0, V_0, K_1, V_1, ... into the ring
+//   warp 1      MMA issuer (the whole warp runs the loop, one elected lane issues):
+//               S_X = Q_X K_j^T into TMEM, O_X += P_X V_j with P read from TMEM
+//   warps 4-7   softmax of tile 0: each thread owns one query row (TMEM lane = row)
+//   warps 8-11  softmax of tile 1
 //
 // The two softmax warpgroups alternate with the tensor core: while one works on its
 // scores the MMA warp computes the other's products.  Running maxima are kept in the
 // base-2 domain and only moved (with a rescale of the TMEM accumulator) when they grow
-// by more than 2^8, so most tiles skip the rescale.
+// by more than 2^8, so most tiles skip the rescale.  At the end of a unit each softmax warp
+// stages its rows of y in shared memory and writes them with TMA stores.
 //
 // Every barrier wait is bounded: on expiry the kernel raises an abort flag, drains the
 // copies and MMAs it issued, frees its tensor memory and records SDPA_ERR_TIMEOUT in a
@@ -458,7 +462,8 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
         if (seq >= C::kStages &&
             !__all_sync(0xffffffffu, mbar_wait_bounded(b_empty(st), ((seq / C::kStages) - 1) & 1, abortp, a.wait_ns)))
           return false;
-        if (leader) {
+        if (leader && SDPA_IN_BOUNDS(w.kv_t0 + tile >= 0 && (int64_t)(w.kv_t0 + tile) * kBN < a.T && st < C::kStages &&
+                                         w.kvh < a.Nkv && w.b < a.B, 101)) {
           mbar_arrive_expect_tx(b_full(st), C::kKVTile);
           int d1, d2, d3;
           perm_coords(a.kv_ds, a.kv_dn, a.kv_db, (w.kv_t0 + tile) * kBN, w.kvh, w.b, d1, d2, d3);
@@ -473,7 +478,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
       // the previous unit's last S MMAs have read its Q tiles
       if (ok && it > 0) ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_qempty, (it - 1) & 1, abortp, a.wait_ns));
       if (!ok) break;
-      if (leader) {
+      if (leader && SDPA_IN_BOUNDS(w.m[0] >= 0 && w.m[0] < a.S && w.m[1] >= 0 && w.qh[0] < a.Nq && w.qh[1] < a.Nq, 102)) {
         mbar_arrive_expect_tx(b_qfull, kQT * C::kQTile);
         for (int x = 0; x < kQT; ++x) {
           int c1, c2, c3;
@@ -678,7 +683,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
       const int mx0 = x == 0 ? w.m[0] : w.m[1];      // first row of this tile
       const int64_t len_b = w.len_b;
       const int64_t i = (int64_t)mx0 + row;          // query row
-      const bool valid = i < a.S;
+      const bool valid = i < a.S && SDPA_IN_BOUNDS(b < a.B && qh < a.Nq && i >= 0, 103);
       int64_t lo = 1, hi = 0;
       if (valid) key_bounds(a, len_b, i, lo, hi);
       // T <= 2^30, so the bounds fit 32 bits once clamped to [-1, T]
@@ -1138,12 +1143,14 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
                 wv[e] = kBF16 ? pack_bf16x2(v0, v1) : pack_f16x2(v0, v1);
               }
               const int c16 = (c & 1) * 4 + q;   // 16-byte piece of the row within the 64 columns
-              st_shared_v4(sY + lane * 128 + ((c16 ^ (lane & 7)) << 4), wv[0], wv[1], wv[2], wv[3]);
+              if (SDPA_IN_BOUNDS(lane * 128 + (c16 << 4) + 16 <= C::kYWarpBytes || kStage, 104))
+                st_shared_v4(sY + lane * 128 + ((c16 ^ (lane & 7)) << 4), wv[0], wv[1], wv[2], wv[3]);
             }
             if ((c & 1) == 1) {
               fence_proxy_async_smem();
               __syncwarp();
-              if (lane == 0) {
+              // a warp whose rows all lie past S has nothing to store
+              if (lane == 0 && mx0 + sub * 32 < a.S && SDPA_IN_BOUNDS(mx0 + sub * 32 >= 0, 105)) {
                 tma_store_4d(&ty, sY, (c >> 1) * 64, yc1, yc2, yc3);
                 bulk_commit();
               }
@@ -1438,5 +1445,7 @@ cudaError_t take_prefill_status(int* status) {
   }
   return e;
 }
+
+SDPA_DEFINE_BOUNDS_TAKE(take_bounds_prefill)
 
 }  // namespace sdpa

@@ -68,7 +68,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const Problem p) 
   for (int64_t j0 = 0; j0 < p.T; j0 += 32) {
     const int64_t j = j0 + lane;
     float s = -INFINITY;
-    if (j < p.T) {
+    if (j < p.T && SDPA_IN_BOUNDS(j >= 0 && kh < p.Nkv && i < p.S, 401)) {
       const T* krow = kv_row<T>(p, false, b, kh, j);
       const bool add_bias = kb && j >= p.P;
       float dot = 0.f;
@@ -95,6 +95,7 @@ __global__ void __launch_bounds__(kWarps * 32) simt_fwd_kernel(const Problem p) 
       const float w = __shfl_sync(0xffffffffu, pj, jj);
       if (w == 0.f) continue;                           // uniform across the warp
       const int64_t jv = j0 + jj;
+      if (!SDPA_IN_BOUNDS(jv < p.T, 402)) continue;
       const T* vrow = kv_row<T>(p, true, b, kh, jv);
       const bool add_bias = vb && jv >= p.P;
 #pragma unroll
@@ -144,5 +145,7 @@ cudaError_t launch_simt_fwd(const Problem& p, sdpa_dtype dt, cudaStream_t st) {
   count_launch();
   return cudaGetLastError();
 }
+
+SDPA_DEFINE_BOUNDS_TAKE(take_bounds_simt)
 
 }  // namespace sdpa

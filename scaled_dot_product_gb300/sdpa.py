@@ -20,6 +20,7 @@ LIB_PATH = os.path.join(_PKG, "libsdpa.so")
 # status codes (include/sdpa.h)
 SDPA_OK = 0
 SDPA_ERR_INVALID = 1
+SDPA_ERR_BOUNDS = 11
 SDPA_ERR_SHAPE = 2
 SDPA_ERR_UNSUPPORTED = 3
 SDPA_ERR_ALIGNMENT = 4
