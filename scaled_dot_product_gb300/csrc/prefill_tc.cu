@@ -80,40 +80,49 @@ __device__ __forceinline__ float tanh_poly(float u) {
   return fmaf(w, q, u);
 }
 
-template <int H, int kQT, bool kMaskStage = false>
+// Shapes of one kernel variant: H = head size of Q and K, HV = head size of V (64 or 128 each).
+template <int H, int HV, int kQT, bool kMaskStage = false>
 struct Cfg {
   static_assert(kQT == 2, "two query tiles per CTA");
-  static constexpr int kRegions = H / 64;              // 128-byte swizzle regions per row
+  static_assert((H == 64 || H == 128) && (HV == 64 || HV == 128), "head sizes");
+  static constexpr int kRegions = H / 64;              // 128-byte swizzle regions per Q / K row
+  static constexpr int kVRegions = HV / 64;            // ... per V row
   static constexpr int kRegionBytes = 128 * 128;       // 128 rows x 128 bytes
   static constexpr int kQTile = kBM * H * 2;
-  static constexpr int kKVTile = kBN * H * 2;
+  static constexpr int kKTile = kBN * H * 2;
+  static constexpr int kVTile = kBN * HV * 2;
+  static constexpr int kKVTile = kKTile > kVTile ? kKTile : kVTile;   // one ring slot
   // Q holds the unit's two tiles; the next unit's tiles load once the current unit's last S
   // MMAs have read them
   static constexpr int kQBuf = kQT * kQTile;
   static constexpr int kQOff = 0;
   static constexpr int kKVOff = kQBuf;
-  // K/V ring depth: what is left of the shared memory; a staged additive mask (H = 64 only)
-  // takes 8 KB per softmax warp out of it
-  static constexpr int kStages = (H == 128) ? 4 : (kMaskStage ? 6 : 10);
   // additive-mask staging: per softmax warp its 32 rows x 128 16-bit columns, 16-byte chunks
   // of row r swizzled by r mod 16
   static constexpr int kMaskWarpBytes = 32 * kBN * 2;
-  static constexpr int kMaskOff = kKVOff + kStages * kKVTile;
   static constexpr int kMaskBytes = kMaskStage ? 4 * kQT * kMaskWarpBytes : 0;
   // output staging for the TMA stores of y: per softmax warp 32 rows x 64 columns (4 KB,
   // 128-byte swizzle); the additive-mask mode reuses the warp's mask region
   static constexpr int kYWarpBytes = 32 * 128;
-  static constexpr int kYOff = kMaskOff + kMaskBytes;
   static constexpr int kYBytes = kMaskStage ? 0 : 4 * kQT * kYWarpBytes;
+  // K/V ring depth: what is left of the shared memory, at most 10 slots, and 6 with a staged
+  // mask, whose ragged last tile is read through L1 (measured: 8 slots left it too little
+  // L1 and were slower)
+  static constexpr int kSmemMax = 232448;
+  static constexpr int kStagesFit = (kSmemMax - 1024 - kQBuf - kMaskBytes - kYBytes) / kKVTile;
+  static constexpr int kStagesCap = kMaskStage ? 6 : 10;
+  static constexpr int kStages = kStagesFit < kStagesCap ? kStagesFit : kStagesCap;
+  static constexpr int kMaskOff = kKVOff + kStages * kKVTile;
+  static constexpr int kYOff = kMaskOff + kMaskBytes;
   static constexpr int kSmem = kYOff + kYBytes + 1024;   // + alignment slack
-  static_assert(kSmem <= 232448, "shared memory");
-  // Tensor memory: S_X (128 columns each), O_X (H columns each) and P_X (16-bit, two per
-  // column: 64 columns).  With H = 128 there is no room for P: P_X overwrites the first 64
+  static_assert(kSmem <= kSmemMax && kStages >= 3, "shared memory");
+  // Tensor memory: S_X (128 columns each), O_X (HV columns each) and P_X (16-bit, two per
+  // column: 64 columns).  With HV = 128 there is no room for P: P_X overwrites the first 64
   // columns of S_X once S_X is in registers.
-  static constexpr bool kAlias = (H == 128);
+  static constexpr bool kAlias = (HV == 128);
   static constexpr int kTmemS0 = 0, kTmemS1 = 128;
-  static constexpr int kTmemO0 = 128 * kQT, kTmemO1 = kTmemO0 + H;
-  static constexpr int kTmemP0 = kAlias ? kTmemS0 : kTmemO0 + kQT * H;
+  static constexpr int kTmemO0 = 128 * kQT, kTmemO1 = kTmemO0 + HV;
+  static constexpr int kTmemP0 = kAlias ? kTmemS0 : kTmemO0 + kQT * HV;
   static constexpr int kTmemP1 = kAlias ? kTmemS1 : kTmemP0 + 64;
   static constexpr uint32_t kTmemCols = 256 * kQT;
 };
@@ -367,15 +376,15 @@ __device__ __forceinline__ void decode_unit(const TcArgs& a, int u, Unit& w) {
   w.n_tiles = (hi_key >= lo_key) ? (int)(hi_key / kBN) - w.kv_t0 + 1 : 0;
 }
 
-template <int H, bool kBF16, int kMode, int SPLIT, bool kStats>
+template <int H, int HV, bool kBF16, int kMode, int SPLIT, bool kStats>
 __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap ty,
                       const TcArgs a) {
   // additive mask through shared memory (H = 64; H = 128 reads it per thread)
-  constexpr bool kStage = (kMode == kAddMask) && (SPLIT == 1) && (H == 64);
+  constexpr bool kStage = (kMode == kAddMask) && (SPLIT == 1) && (H == 64) && (HV == 64);
   constexpr int kQT = 2;
-  using C = Cfg<H, kQT, kStage>;
+  using C = Cfg<H, HV, kQT, kStage>;
   using Lay = Layout<kQT, SPLIT>;
   constexpr int kSplit = SPLIT;                     // softmax threads per query row
   constexpr int kHalf = kBN / kSplit;               // score columns per softmax thread
@@ -464,10 +473,11 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
           return false;
         if (leader && SDPA_IN_BOUNDS(w.kv_t0 + tile >= 0 && (int64_t)(w.kv_t0 + tile) * kBN < a.T && st < C::kStages &&
                                          w.kvh < a.Nkv && w.b < a.B, 101)) {
-          mbar_arrive_expect_tx(b_full(st), C::kKVTile);
+          const bool is_v = map == &tv;
+          mbar_arrive_expect_tx(b_full(st), is_v ? C::kVTile : C::kKTile);
           int d1, d2, d3;
           perm_coords(a.kv_ds, a.kv_dn, a.kv_db, (w.kv_t0 + tile) * kBN, w.kvh, w.b, d1, d2, d3);
-          for (int r = 0; r < C::kRegions; ++r)
+          for (int r = 0; r < (is_v ? C::kVRegions : C::kRegions); ++r)
             tma_load_4d(sKV + st * C::kKVTile + r * C::kRegionBytes, map, b_full(st), 64 * r, d1, d2, d3);
         }
         ++seq;
@@ -519,7 +529,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
       return __all_sync(0xffffffffu, mbar_wait_bounded(bar, parity, abortp, a.wait_ns));
     };
     constexpr uint32_t kIdQK = idesc_f16(kBF16, kBM, kBN, false);
-    constexpr uint32_t kIdPV = idesc_f16(kBF16, kBM, H, true);
+    constexpr uint32_t kIdPV = idesc_f16(kBF16, kBM, HV, true);
     const uint32_t tS[2] = {tmem + C::kTmemS0, tmem + C::kTmemS1};
     const uint32_t tO[2] = {tmem + C::kTmemO0, tmem + C::kTmemO1};
     const uint32_t tP[2] = {tmem + C::kTmemP0, tmem + C::kTmemP1};
@@ -659,7 +669,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
     const int pair_bar = 1 + x * 4 + sub;           // named barrier of the warps of these rows
     const uint32_t trow = tmem + ((uint32_t)(sub * 32) << 16);
     const uint32_t tS = trow + (x == 0 ? C::kTmemS0 : C::kTmemS1) + kHalf * hh;
-    const uint32_t tO = trow + (x == 0 ? C::kTmemO0 : C::kTmemO1) + (H / kSplit) * hh;
+    const uint32_t tO = trow + (x == 0 ? C::kTmemO0 : C::kTmemO1) + (HV / kSplit) * hh;
     const uint32_t tP = trow + (x == 0 ? C::kTmemP0 : C::kTmemP1) + (kHalf / 2) * hh;
     const uint32_t sMask = sbase + C::kMaskOff + (uint32_t)(x * 4 + sub) * C::kMaskWarpBytes;
     // log2-domain factor applied inside the exponent: raw scores (plain mode) carry the
@@ -1043,7 +1053,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
             // that kept their maximum)
             const f2_t c2 = f2_pack(corr, corr);
 #pragma unroll
-            for (int c = 0; c < H / (32 * kSplit); ++c) {
+            for (int c = 0; c < HV / (32 * kSplit); ++c) {
               uint32_t o[32];
               tmem_ld32(tO + c * 32, o);
               tmem_ld_wait();
@@ -1093,7 +1103,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
         denom += ex2_approx(Elem<T>::to_f32(reinterpret_cast<const T*>(a.head_sink)[qh]) * kLog2e - m_use);
       const float inv = (denom > 0.f && m_use != -INFINITY) ? 1.f / denom : 0.f;
       T* yrow = reinterpret_cast<T*>(a.y) + (int64_t)b * a.y_sb + (int64_t)qh * a.y_sh + i * a.y_ss +
-                (H / kSplit) * hh;
+                (HV / kSplit) * hh;
       // y through shared memory: the warp's 32 rows, 64 columns at a time, one TMA store each
       // (rows past S are clipped by the tensor map); a unit with no admitted key writes its
       // zero rows directly
@@ -1107,7 +1117,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
                              : nullptr;
       float delta = 0.f;
 #pragma unroll
-      for (int c = 0; c < H / (32 * kSplit); ++c) {
+      for (int c = 0; c < HV / (32 * kSplit); ++c) {
         uint32_t o[32];
         if (n_tiles > 0) {
           tmem_ld32(tO + c * 32, o);
@@ -1256,20 +1266,20 @@ int sm_count() {
   return n;
 }
 
-template <int H, bool kBF16, int kMode, int SPLIT, bool kStats = false>
+template <int H, int HV, bool kBF16, int kMode, int SPLIT, bool kStats = false>
 cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& ty,
                         TcArgs a, cudaStream_t st) {
-  using C = Cfg<H, 2, (kMode == kAddMask) && (SPLIT == 1) && (H == 64)>;
+  using C = Cfg<H, HV, 2, (kMode == kAddMask) && (SPLIT == 1) && (H == 64) && (HV == 64)>;
   using Lay = Layout<2, SPLIT>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, kBF16, kMode, SPLIT, kStats>,
+    attr_err = cudaFuncSetAttribute(prefill_tc_kernel<H, HV, kBF16, kMode, SPLIT, kStats>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     // the in-kernel register split assumes the block is launched with kLaunchRegs per
     // thread; with fewer, the softmax warps' request could never be met
     cudaFuncAttributes fa{};
-    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<H, kBF16, kMode, SPLIT, kStats>);
+    if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<H, HV, kBF16, kMode, SPLIT, kStats>);
     if (attr_err == cudaSuccess && fa.numRegs < Lay::kLaunchRegs) attr_err = cudaErrorLaunchOutOfResources;
   });
   if (attr_err != cudaSuccess) return attr_err;
@@ -1278,7 +1288,7 @@ cudaError_t launch_mode(const CUtensorMap& tq, const CUtensorMap& tk, const CUte
   const int sms = sm_count();
   if (sms <= 0) return cudaErrorInvalidDevice;
   const int grid = std::min(a.nunits, sms);
-  prefill_tc_kernel<H, kBF16, kMode, SPLIT, kStats><<<(unsigned)grid, Lay::kThreads, C::kSmem, st>>>(tq, tk, tv, ty, a);
+  prefill_tc_kernel<H, HV, kBF16, kMode, SPLIT, kStats><<<(unsigned)grid, Lay::kThreads, C::kSmem, st>>>(tq, tk, tv, ty, a);
   count_launch(1);
   return cudaGetLastError();
 }
@@ -1292,17 +1302,27 @@ cudaError_t launch_t(const CUtensorMap& tq, const CUtensorMap& tk, const CUtenso
     // the backward's statistics pass, in the rule mode of the problem (no softcap: the
     // backward rejects it)
     if (a.has_softcap) return cudaErrorInvalidValue;
-    if (a.generic) return launch_mode<H, kBF16, kGeneric, 1, true>(tq, tk, tv, ty, a, st);
-    if (a.add_fast) return launch_mode<H, kBF16, kAddMask, 1, true>(tq, tk, tv, ty, a, st);
-    if (a.keep_fast) return launch_mode<H, kBF16, kKeep, 1, true>(tq, tk, tv, ty, a, st);
-    return launch_mode<H, kBF16, kPlain, 1, true>(tq, tk, tv, ty, a, st);
+    if (a.generic) return launch_mode<H, H, kBF16, kGeneric, 1, true>(tq, tk, tv, ty, a, st);
+    if (a.add_fast) return launch_mode<H, H, kBF16, kAddMask, 1, true>(tq, tk, tv, ty, a, st);
+    if (a.keep_fast) return launch_mode<H, H, kBF16, kKeep, 1, true>(tq, tk, tv, ty, a, st);
+    return launch_mode<H, H, kBF16, kPlain, 1, true>(tq, tk, tv, ty, a, st);
   }
-  if (a.generic) return launch_mode<H, kBF16, kGeneric, 1>(tq, tk, tv, ty, a, st);
-  if (a.keep_fast) return launch_mode<H, kBF16, kKeep, 1>(tq, tk, tv, ty, a, st);
-  if (a.add_fast) return launch_mode<H, kBF16, kAddMask, 1>(tq, tk, tv, ty, a, st);
+  if (a.generic) return launch_mode<H, H, kBF16, kGeneric, 1>(tq, tk, tv, ty, a, st);
+  if (a.keep_fast) return launch_mode<H, H, kBF16, kKeep, 1>(tq, tk, tv, ty, a, st);
+  if (a.add_fast) return launch_mode<H, H, kBF16, kAddMask, 1>(tq, tk, tv, ty, a, st);
   if constexpr (kBF16)
-    if (a.cap_fixed) return launch_mode<H, kBF16, kCapFixed, 1>(tq, tk, tv, ty, a, st);
-  return launch_mode<H, kBF16, kPlain, 1>(tq, tk, tv, ty, a, st);
+    if (a.cap_fixed) return launch_mode<H, H, kBF16, kCapFixed, 1>(tq, tk, tv, ty, a, st);
+  return launch_mode<H, H, kBF16, kPlain, 1>(tq, tk, tv, ty, a, st);
+}
+
+// A value head size different from the query/key one: the interval-rule mode when only
+// structural rules (and softcap) apply, the per-element mode for everything else.
+template <int H, int HV, bool kBF16>
+cudaError_t launch_hv(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& ty,
+                      const TcArgs& a, cudaStream_t st) {
+  if (a.lse2_out) return cudaErrorInvalidValue;   // the backward takes H == Hv
+  if (a.generic || a.keep_fast || a.add_fast) return launch_mode<H, HV, kBF16, kGeneric, 1>(tq, tk, tv, ty, a, st);
+  return launch_mode<H, HV, kBF16, kPlain, 1>(tq, tk, tv, ty, a, st);
 }
 
 }  // namespace
@@ -1328,7 +1348,7 @@ bool tc_same_axis_order(const View& k, const View& v, int64_t B, int64_t N, int6
 
 bool tc_eligible(const Problem& p, sdpa_dtype dt) {
   if (dt != SDPA_F16 && dt != SDPA_BF16) return false;
-  if (p.H != p.Hv || (p.H != 64 && p.H != 128)) return false;
+  if ((p.H != 64 && p.H != 128) || (p.Hv != 64 && p.Hv != 128)) return false;
   if (p.T < 1 || p.S < 16) return false;
   if (p.T > (int64_t)1 << 30 || p.r.window > (int64_t)1 << 30) return false;
   for (const View* v : {&p.q, &p.k, &p.v})
@@ -1419,6 +1439,19 @@ cudaError_t launch_prefill_tc_stats(const Problem& p, sdpa_dtype dt, float* lse2
   if (units > 0x7fffffff) return cudaErrorInvalidValue;
   a.nunits = (int)units;
   const bool bf = dt == SDPA_BF16;
+  if (p.H != p.Hv) {
+    if (a.keep_fast || a.add_fast) {   // per-element rules: the keep / additive-mask fast paths need H == Hv
+      a.generic = 1;
+      a.keep_fast = a.add_fast = 0;
+    }
+    a.cap_fixed = 0;
+    if (p.H == 64) {
+      *name = bf ? "prefill_tc_bf16_h64_hv128" : "prefill_tc_f16_h64_hv128";
+      return bf ? launch_hv<64, 128, true>(tq, tk, tv, ty, a, st) : launch_hv<64, 128, false>(tq, tk, tv, ty, a, st);
+    }
+    *name = bf ? "prefill_tc_bf16_h128_hv64" : "prefill_tc_f16_h128_hv64";
+    return bf ? launch_hv<128, 64, true>(tq, tk, tv, ty, a, st) : launch_hv<128, 64, false>(tq, tk, tv, ty, a, st);
+  }
   if (p.H == 128) {
     *name = bf ? "prefill_tc_bf16_h128" : "prefill_tc_f16_h128";
     return bf ? launch_t<128, true>(tq, tk, tv, ty, a, st) : launch_t<128, false>(tq, tk, tv, ty, a, st);

@@ -177,8 +177,30 @@ def test_empty_batch_and_empty_query_write_present_only():
 
 def test_head_size_256_and_distinct_value_width():
     run_and_compare(make_case("h256", dtype=torch.bfloat16, B=1, Nq=2, S=70, L=90, H=256, seed=14), "fwd")
-    run_and_compare(make_case("hv", dtype=torch.float16, B=1, Nq=4, Nkv=2, S=33, L=70, H=64, Hv=128,
-                              seed=15, causal="lower_right"), "fwd")
+    err, name = run_and_compare(make_case("hv", dtype=torch.float16, B=1, Nq=4, Nkv=2, S=33, L=70, H=64, Hv=128,
+                                          seed=15, causal="lower_right"), "fwd")
+    assert name.startswith("prefill_tc"), name
+
+
+@pytest.mark.parametrize("kw", [
+    dict(name="h64_hv128_gqa_causal_bf16", dtype=torch.bfloat16, H=64, Hv=128, Nkv=2, causal="upper_left",
+         len_kind="nonpad", len_range=(150, 300)),
+    dict(name="h128_hv64_window_sink_f16", dtype=torch.float16, H=128, Hv=64, causal="lower_right", window=70,
+         sink=True),
+    dict(name="h128_hv64_addmask_bf16", dtype=torch.bfloat16, H=128, Hv=64, add_mask="float",
+         add_mask_shape=(2, 1, 260, 300)),
+    dict(name="h64_hv128_bool_f16", dtype=torch.float16, H=64, Hv=128, keep_kind="bool",
+         keep_mask_shape=(2, 4, 260, 300)),
+    dict(name="h64_hv128_softcap_bf16", dtype=torch.bfloat16, H=64, Hv=128, causal="upper_left", softcap=20.0),
+])
+def test_distinct_value_width_tensor_core(kw):
+    """Value head size different from the query/key one (64 / 128) on the tensor-core kernel."""
+    kw = dict(kw)
+    name = kw.pop("name")
+    kw.setdefault("Nkv", 4)
+    case = make_case(name, B=2, Nq=4, S=260, L=300, seed=80 + len(name), q_layout="bsnh", **kw)
+    err, kernel = run_and_compare(case, "fwd")
+    assert kernel.startswith("prefill_tc") and "_hv" in kernel, kernel
 
 
 def test_softcap_after_bias_reading():
