@@ -58,7 +58,9 @@ struct Layout {
 #ifndef SDPA_CTL_REGS_SMALL
 #define SDPA_CTL_REGS_SMALL 56
 #endif
-  static constexpr int kCtlRegs = (kLaunchRegs <= 96) ? SDPA_CTL_REGS_SMALL : ((QT == 1) ? 64 : 80);
+  // (88 with two tiles: the MMA warp's descriptors and counters fit without spilling, and the
+  // softmax warpgroups keep 208)
+  static constexpr int kCtlRegs = (kLaunchRegs <= 96) ? SDPA_CTL_REGS_SMALL : ((QT == 1) ? 64 : 88);
   static constexpr int kSmxRegs = ((kLaunchRegs * kThreads - kCtlRegs * 128) / kSmxThreads) & ~7;
   static_assert(kSmxRegs <= 256 && kSmxRegs >= kLaunchRegs, "register split");
   static_assert(kCtlRegs * 128 + kSmxRegs * kSmxThreads <= kLaunchRegs * kThreads, "register split");
@@ -594,7 +596,10 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
       }
       if constexpr (C::kAlias) {
         // P_X(j) lives in S_X's columns: PV_X(j) first, then S_X(j+1); one commit on
-        // sfull_X then also tells softmax X that O_X holds PV_X(j)
+        // sfull_X then also tells softmax X that O_X holds PV_X(j).  The unit's last PV_X
+        // commits on odone_X instead: the next unit's S_X(0) follows it without waiting for
+        // the softmax, and a second sfull_X phase completing before the epilogue's wait
+        // would leave that wait on the wrong parity.
         for (int j = 0; j < n && ok; ++j) {
           const bool more = j + 1 < n;
           const int vst = seq % C::kStages;
@@ -608,8 +613,10 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
             if (more) {
               if (x == 0 && !(ok = wait_full(seq))) break;
               issue_S(x, kst);
+              commit(b_sfull(x));
+            } else {
+              commit(b_odone(x));
             }
-            commit(b_sfull(x));
           }
           if (!ok) break;
           ++np;
@@ -1081,15 +1088,10 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
       if (!ok) break;
 
       // ---- epilogue: O / (l + sink term), rounded once to the output type.  The last PV of
-      // the unit must be done (with P aliasing S, its sfull commit says so).
+      // the unit must be done (its odone commit).
       if (n_tiles > 0) {
-        if constexpr (C::kAlias) {
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_sfull(x), cs & 1, abortp, a.wait_ns));
-          ++cs;
-        } else {
-          ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_odone(x), co & 1, abortp, a.wait_ns));
-          ++co;
-        }
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_odone(x), co & 1, abortp, a.wait_ns));
+        ++co;
         if (!ok) break;
       }
       tc_fence_after();
