@@ -826,8 +826,11 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
           const float amax = fmax3(fmax3(am8[0], am8[1], am8[2]), fmax3(am8[3], am8[4], am8[5]), fmaxf(am8[6], am8[7]));
           const float negm = -m_use;
           const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
-          if (amax <= a.fx_lim && full) {
-            // every key admitted: exponent and weight in one pass, in place
+          if (amax <= a.fx_lim) {
+            // exponent and weight in one pass, in place.  Tiles with excluded keys (the causal
+            // diagonal, a length boundary) run the same pass, whose code the full tiles keep
+            // hot, then set the excluded weights to 0: every score of the tile is finite and
+            // inside the cubic's range, so the pass is defined for every key.
             const f2_t ca = f2_pack(a.fx_a, a.fx_a), cb = f2_pack(a.fx_b, a.fx_b), nm2 = f2_pack(negm, negm);
 #pragma unroll
             for (int e = 0; e < kHalf; e += 2) {
@@ -838,20 +841,16 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
               s[e] = ex2_approx(z0);
               s[e + 1] = ex2_approx(z1);
             }
-            weights = true;
-          } else if (amax <= a.fx_lim) {
-            // some keys excluded (the causal diagonal, a length boundary): the same single
-            // pass, an excluded key's exponent replaced by -inf (weight 0)
-            const f2_t ca = f2_pack(a.fx_a, a.fx_a), cb = f2_pack(a.fx_b, a.fx_b), nm2 = f2_pack(negm, negm);
-            const int elo = lo32 - key0, ehi = hi32 - key0;
+            if (!full) {
+              const int elo = lo32 - key0, ehi = hi32 - key0;
+              if (ehi < kHalf - 1) {
 #pragma unroll
-            for (int e = 0; e < kHalf; e += 2) {
-              const f2_t x2 = f2_pack(s[e], s[e + 1]);
-              const f2_t tt = f2_fma(f2_mul(x2, x2), cb, ca);
-              float z0, z1;
-              f2_unpack(f2_fma(x2, tt, nm2), z0, z1);
-              s[e] = ex2_approx((e >= elo && e <= ehi) ? z0 : -INFINITY);
-              s[e + 1] = ex2_approx((e + 1 >= elo && e + 1 <= ehi) ? z1 : -INFINITY);
+                for (int e = 0; e < kHalf; ++e) s[e] = (e <= ehi) ? s[e] : 0.f;
+              }
+              if (elo > 0) {
+#pragma unroll
+                for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo) ? s[e] : 0.f;
+              }
             }
             weights = true;
           } else {
