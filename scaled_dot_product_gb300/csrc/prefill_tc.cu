@@ -82,6 +82,22 @@ __device__ __forceinline__ float tanh_poly(float u) {
   return fmaf(w, q, u);
 }
 
+// Keys outside the admitted interval [elo, ehi] of a row's tile segment (element indices) take
+// the value fill.  Per 32-column chunk the admitted keys are formed once as a bit set, so each
+// key then costs one bit test and one select, with no branches (branches that overwrite parts
+// of the score array cost registers in the softmax warps).
+template <int N>
+__device__ __forceinline__ void clip_interval(float (&s)[N], int elo, int ehi, float fill) {
+#pragma unroll
+  for (int c0 = 0; c0 < N; c0 += 32) {
+    const int lo = max(elo - c0, 0), hi = min(ehi - c0, 31);
+    const uint32_t up = 0xffffffffu >> (31 - max(hi, 0));   // bits 0 .. hi
+    const uint32_t m = (lo <= hi) ? (up & (0xffffffffu << min(lo, 31))) : 0u;
+#pragma unroll
+    for (int e = 0; e < 32; ++e) s[c0 + e] = ((m >> e) & 1u) ? s[c0 + e] : fill;
+  }
+}
+
 // Shapes of one kernel variant: H = head size of Q and K, HV = head size of V (64 or 128 each).
 template <int H, int HV, int kQT, bool kMaskStage = false>
 struct Cfg {
@@ -842,6 +858,8 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
               s[e + 1] = ex2_approx(z1);
             }
             if (!full) {
+              // a suffix (causal diagonal, length boundary) and a prefix (window start) of
+              // excluded keys, each with one compare and one select per key
               const int elo = lo32 - key0, ehi = hi32 - key0;
               if (ehi < kHalf - 1) {
 #pragma unroll
@@ -856,11 +874,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
           } else {
 #pragma unroll
             for (int e = 0; e < kHalf; ++e) s[e] = fmaf(a.cap_out_log2, tanh_approx(s[e] * a.cap_in), negm);
-            if (!full) {
-              const int elo = lo32 - key0, ehi = hi32 - key0;
-#pragma unroll
-              for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
-            }
+            if (!full) clip_interval(s, lo32 - key0, hi32 - key0, -INFINITY);
           }
         } else if constexpr (kMode == kPlain) {
           const bool full = (lo32 <= key0) && (key0 + kHalf - 1 <= hi32);
@@ -903,11 +917,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
               for (int e = 0; e < kHalf; ++e) s[e] = tanh_approx(s[e]);
             }
           }
-          if (!full) {
-            const int elo = lo32 - key0, ehi = hi32 - key0;
-#pragma unroll
-            for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
-          }
+          if (!full) clip_interval(s, lo32 - key0, hi32 - key0, -INFINITY);
         } else if constexpr (kMode == kKeep) {
           // raw scores: a key the keep mask drops is excluded (bool) or gets the filter value
           // (binary), as does every key at or past a key-padding length; then the bounds
@@ -915,16 +925,34 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
           const bool all_keep = (kb[0] & kb[1] & kb[2] & kb[3]) == 0xffffffffu;
           const int len_e = (a.r.len_kind == SDPA_LEN_KEYLEN_I32) ? (int)max64(-1, min64(len_b - key0, kHalf)) : kHalf;
           if (!__all_sync(0xffffffffu, full && all_keep && len_e >= kHalf)) {
-            const bool drop_excludes = a.r.keep_kind == SDPA_KEEP_BOOL_U8;
             const float fr = a.filter_raw;
-            const int elo = lo32 - key0, ehi = hi32 - key0;
+            // dropped keys: one bit test and one predicated update per key
+            if (!all_keep) {
+              if (a.r.keep_kind == SDPA_KEEP_BOOL_U8) {
 #pragma unroll
-            for (int e = 0; e < kHalf; ++e) {
-              float v = s[e];
-              if (!((kb[e >> 5] >> (e & 31)) & 1u)) v = drop_excludes ? -INFINITY : v + fr;
-              if (e >= len_e) v += fr;
-              s[e] = (e >= elo && e <= ehi) ? v : -INFINITY;
+                for (int e = 0; e < kHalf; ++e)
+                  if (!((kb[e >> 5] >> (e & 31)) & 1u)) s[e] = -INFINITY;
+              } else {
+#pragma unroll
+                for (int e = 0; e < kHalf; ++e)
+                  if (!((kb[e >> 5] >> (e & 31)) & 1u)) s[e] += fr;
+              }
             }
+            // keys at or past the key-padding length, 32 columns at a time
+            if (len_e < kHalf) {
+#pragma unroll
+              for (int c0 = 0; c0 < kHalf; c0 += 32) {
+                if (len_e <= c0) {
+#pragma unroll
+                  for (int e = c0; e < c0 + 32; ++e) s[e] += fr;
+                } else if (len_e < c0 + 32) {
+#pragma unroll
+                  for (int e = c0; e < c0 + 32; ++e)
+                    if (e >= len_e) s[e] += fr;
+                }
+              }
+            }
+            if (!full) clip_interval(s, lo32 - key0, hi32 - key0, -INFINITY);
           }
         } else if constexpr (kMode == kAddMask) {
           // additive mask / attention bias, then softcap (or the reverse), then the bounds;
@@ -966,11 +994,7 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
             const float cap = a.r.softcap, cin = a.cap_in;
             run([cap, cin](float sv, float mv) { return fmaf(cap, tanh_approx(sv * cin), mv); });
           }
-          if (!((lo32 <= key0) && (key0 + kHalf - 1 <= hi32))) {
-            const int elo = lo32 - key0, ehi = hi32 - key0;
-#pragma unroll
-            for (int e = 0; e < kHalf; ++e) s[e] = (e >= elo && e <= ehi) ? s[e] : -INFINITY;
-          }
+          if (!((lo32 <= key0) && (key0 + kHalf - 1 <= hi32))) clip_interval(s, lo32 - key0, hi32 - key0, -INFINITY);
         } else {
 #pragma unroll
           for (int e = 0; e < kHalf; ++e) {
