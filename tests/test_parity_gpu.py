@@ -345,3 +345,37 @@ def test_keep_mask_excluding_whole_rows_gives_zeros():
     c = make_case("bool_allfalse", dtype=torch.bfloat16, B=1, Nq=2, S=150, L=150, H=64, seed=71,
                   keep_kind="bool", keep_mask_shape=(1, 1, 150, 150), keep_density=0.0)
     run_and_compare(c, "fwd")
+
+
+# ----------------------------------------------------------------- many launches, barrier phases
+
+@pytest.mark.parametrize("kw", [
+    # P aliasing S (Hv = 128): the unit's last P.V and the next unit's first S complete back to
+    # back; the epilogue must wait on its own barrier, not on a second phase of the score one
+    dict(name="stress_keep_f16_h128", dtype=torch.float16, B=2, Nq=16, Nkv=16, S=1024, L=1024, H=128,
+         q_layout="bsnh", kv_layout="bsnh", causal="lower_right", keep_kind="filter",
+         keep_mask_shape=(2, 1, 1024, 1024), seed=91),
+    dict(name="stress_capfix_bf16_h128", dtype=torch.bfloat16, B=2, Nq=16, Nkv=4, S=1024, L=1024, H=128,
+         causal="upper_left", softcap=30.0, len_kind="nonpad", len_range=(600, 1024), seed=92),
+    dict(name="stress_plain_bf16_h64", dtype=torch.bfloat16, B=1, Nq=32, Nkv=4, S=2048, L=2048, H=64,
+         causal="lower_right", window=512, sink=True, seed=93),
+])
+def test_many_launches_keep_every_barrier_phase(kw):
+    """Hundreds of back-to-back launches of the persistent kernel (several units per CTA):
+    every one completes without a bounded wait expiring, and the last result matches the
+    oracle on sampled rows."""
+    c = make_case(**kw)
+    d = c.to("cuda")
+    ws = sdpa.case_workspace(d, "fwd")
+    outs = sdpa.case_outputs(d)
+    for _ in range(400):
+        sdpa.run_case(d, "fwd", outputs=outs, workspace=ws)
+    torch.cuda.synchronize()
+    assert sdpa.sdpa_query_status() == sdpa.SDPA_OK, sdpa.sdpa_last_error()
+    assert sdpa.sdpa_last_kernel_name().startswith("prefill_tc"), sdpa.sdpa_last_kernel_name()
+    got = y_as_bnsh(c, outs[0])
+    rng = np.random.default_rng(7)
+    rows = np.stack([rng.integers(0, c.B, 64), rng.integers(0, c.Nq, 64), rng.integers(0, c.S, 64)], 1)
+    want, _ = oracle.attention_rows(problem(c), rows)
+    err = np.abs(got[rows[:, 0], rows[:, 1], rows[:, 2]] - want).max()
+    assert err <= TOL[c.dtype], f"{c.name}: max-abs error {err:.3e}"
