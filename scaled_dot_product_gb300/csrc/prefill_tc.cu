@@ -705,8 +705,130 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
     int co = 0;   // odone phases waited
     int it = 0;   // units with work
     bool ok = true;
+    // the unit whose epilogue is pending (e_real false: the dry pass before the first unit,
+    // run in the interval-rule and softcap modes, where it measured faster; the mask modes
+    // start their first unit at once)
+    constexpr bool kPrimeEpilogue = (kMode == kPlain || kMode == kCapFixed);
+    bool e_real = false;
+    int e_tiles = 1, e_b = 0, e_qh = 0, e_mx0 = 0;
+    float e_l = 0.f, e_m = -INFINITY;
+    bool e_valid = false;
+    int64_t e_i = 0;
     for (int ku = 0; ok; ++ku) {
       const int u = unit_at(ku, cta, G);
+      if (e_real || kPrimeEpilogue) {
+        const int n_tiles = e_tiles;
+        const float l = e_l, m_use = e_m;
+        const bool valid = e_valid;
+        const int64_t i = e_i;
+        const int b = e_b, qh = e_qh, mx0 = e_mx0;
+        // ---- epilogue of the previous unit: O / (l + sink term), rounded once to the output
+        // type; its last PV must be done (its odone commit).  Before the first unit the same code
+        // runs once as a dry pass (no waits, nothing stored, results discarded): the CTA waits
+        // for its first Q and K tiles then anyway, and the pass brings the epilogue's code into
+        // the caches, where the first real epilogue, which every CTA reaches at about the same
+        // time, would otherwise fetch it from memory.
+        if (e_real && n_tiles > 0) {
+          ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_odone(x), co & 1, abortp, a.wait_ns));
+          ++co;
+          if (!ok) break;
+        }
+        tc_fence_after();
+        float denom = l;
+        if constexpr (kSplit == 2) {
+          red_sum[x][hh][row] = l;
+          named_bar_sync(pair_bar, 64);
+          denom += red_sum[x][hh ^ 1][row];
+        }
+        if (a.head_sink && m_use != -INFINITY)
+          denom += ex2_approx(Elem<T>::to_f32(reinterpret_cast<const T*>(a.head_sink)[qh]) * kLog2e - m_use);
+        const float inv = (denom > 0.f && m_use != -INFINITY) ? 1.f / denom : 0.f;
+        T* yrow = reinterpret_cast<T*>(a.y) + (int64_t)b * a.y_sb + (int64_t)qh * a.y_sh + i * a.y_ss +
+                  (HV / kSplit) * hh;
+        // y through shared memory: the warp's 32 rows, 64 columns at a time, one TMA store each
+        // (rows past S are clipped by the tensor map); a unit with no admitted key writes its
+        // zero rows directly
+        const bool write_y = !kStats || a.y != nullptr;
+        const uint32_t sY = kStage ? sMask : sbase + C::kYOff + (uint32_t)(x * 4 + sub) * C::kYWarpBytes;
+        int yc1 = 0, yc2 = 0, yc3 = 0;
+        if (write_y && n_tiles > 0) perm_coords(a.y_ds, a.y_dn, a.y_db, mx0 + sub * 32, qh, b, yc1, yc2, yc3);
+        constexpr bool stats = kStats && kSplit == 1;   // the backward's statistics pass
+        const T* dyrow = stats ? reinterpret_cast<const T*>(a.dy) + (int64_t)b * a.dy_sb + (int64_t)qh * a.dy_sh +
+                                     i * a.dy_ss
+                               : nullptr;
+        float delta = 0.f;
+  #pragma unroll
+        for (int c = 0; c < HV / (32 * kSplit); ++c) {
+          uint32_t o[32];
+          if (n_tiles > 0) {
+            tmem_ld32(tO + c * 32, o);
+            tmem_ld_wait();
+          } else {
+  #pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = 0u;
+          }
+          if (stats && valid) {
+            // delta = dY . O with O = o / denom in fp32
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const uint4 uv = *reinterpret_cast<const uint4*>(dyrow + c * 32 + q * 8);
+              const T* e8 = reinterpret_cast<const T*>(&uv);
+  #pragma unroll
+              for (int e = 0; e < 8; ++e) delta = fmaf(Elem<T>::to_f32(e8[e]), __uint_as_float(o[q * 8 + e]) * inv, delta);
+            }
+          }
+          if (n_tiles > 0) {
+            if (write_y) {
+              if ((c & 1) == 0) {
+                // the warp's previous store has finished reading the staging buffer
+                if (lane == 0) bulk_wait_read<0>();
+                __syncwarp();
+              }
+  #pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                uint32_t wv[4];
+  #pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const float v0 = __uint_as_float(o[q * 8 + 2 * e]) * inv;
+                  const float v1 = __uint_as_float(o[q * 8 + 2 * e + 1]) * inv;
+                  wv[e] = kBF16 ? pack_bf16x2(v0, v1) : pack_f16x2(v0, v1);
+                }
+                const int c16 = (c & 1) * 4 + q;   // 16-byte piece of the row within the 64 columns
+                if (SDPA_IN_BOUNDS(lane * 128 + (c16 << 4) + 16 <= C::kYWarpBytes || kStage, 104))
+                  st_shared_v4(sY + lane * 128 + ((c16 ^ (lane & 7)) << 4), wv[0], wv[1], wv[2], wv[3]);
+              }
+              if ((c & 1) == 1) {
+                fence_proxy_async_smem();
+                __syncwarp();
+                // a warp whose rows all lie past S has nothing to store
+                if (e_real && lane == 0 && mx0 + sub * 32 < a.S && SDPA_IN_BOUNDS(mx0 + sub * 32 >= 0, 105)) {
+                  tma_store_4d(&ty, sY, (c >> 1) * 64, yc1, yc2, yc3);
+                  bulk_commit();
+                }
+              }
+            }
+          } else if (valid && write_y) {
+  #pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              uint32_t wv[4];
+  #pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float v0 = __uint_as_float(o[q * 8 + 2 * e]) * inv;
+                const float v1 = __uint_as_float(o[q * 8 + 2 * e + 1]) * inv;
+                wv[e] = kBF16 ? pack_bf16x2(v0, v1) : pack_f16x2(v0, v1);
+              }
+              *reinterpret_cast<uint4*>(yrow + c * 32 + q * 8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
+            }
+          }
+        }
+        if (stats && valid) {
+          const int64_t r_idx = ((int64_t)b * a.Nq + qh) * a.S + i;
+          a.lse2_out[r_idx] = (denom > 0.f && m_use != -INFINITY) ? m_use + log2f(denom) : INFINITY;
+          a.delta_out[r_idx] = delta;
+        }
+        // the epilogue's tensor-memory reads are complete before this thread's next P store,
+        // which the MMA warp waits for before the next unit's first PV overwrites O
+      }
       if (u >= a.nunits) break;
       Unit w;
       decode_unit(a, u, w);
@@ -1110,108 +1232,16 @@ __global__ void __launch_bounds__(Layout<2, SPLIT>::kThreads, 1)
       if constexpr (kStage) ptx::cp_async_wait_all();
       if (!ok) break;
 
-      // ---- epilogue: O / (l + sink term), rounded once to the output type.  The last PV of
-      // the unit must be done (its odone commit).
-      if (n_tiles > 0) {
-        ok = __all_sync(0xffffffffu, mbar_wait_bounded(b_odone(x), co & 1, abortp, a.wait_ns));
-        ++co;
-        if (!ok) break;
-      }
-      tc_fence_after();
-      float denom = l;
-      if constexpr (kSplit == 2) {
-        red_sum[x][hh][row] = l;
-        named_bar_sync(pair_bar, 64);
-        denom += red_sum[x][hh ^ 1][row];
-      }
-      if (a.head_sink && m_use != -INFINITY)
-        denom += ex2_approx(Elem<T>::to_f32(reinterpret_cast<const T*>(a.head_sink)[qh]) * kLog2e - m_use);
-      const float inv = (denom > 0.f && m_use != -INFINITY) ? 1.f / denom : 0.f;
-      T* yrow = reinterpret_cast<T*>(a.y) + (int64_t)b * a.y_sb + (int64_t)qh * a.y_sh + i * a.y_ss +
-                (HV / kSplit) * hh;
-      // y through shared memory: the warp's 32 rows, 64 columns at a time, one TMA store each
-      // (rows past S are clipped by the tensor map); a unit with no admitted key writes its
-      // zero rows directly
-      const bool write_y = !kStats || a.y != nullptr;
-      const uint32_t sY = kStage ? sMask : sbase + C::kYOff + (uint32_t)(x * 4 + sub) * C::kYWarpBytes;
-      int yc1 = 0, yc2 = 0, yc3 = 0;
-      if (write_y && n_tiles > 0) perm_coords(a.y_ds, a.y_dn, a.y_db, mx0 + sub * 32, qh, b, yc1, yc2, yc3);
-      constexpr bool stats = kStats && kSplit == 1;   // the backward's statistics pass
-      const T* dyrow = stats ? reinterpret_cast<const T*>(a.dy) + (int64_t)b * a.dy_sb + (int64_t)qh * a.dy_sh +
-                                   i * a.dy_ss
-                             : nullptr;
-      float delta = 0.f;
-#pragma unroll
-      for (int c = 0; c < HV / (32 * kSplit); ++c) {
-        uint32_t o[32];
-        if (n_tiles > 0) {
-          tmem_ld32(tO + c * 32, o);
-          tmem_ld_wait();
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
-        if (stats && valid) {
-          // delta = dY . O with O = o / denom in fp32
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 uv = *reinterpret_cast<const uint4*>(dyrow + c * 32 + q * 8);
-            const T* e8 = reinterpret_cast<const T*>(&uv);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) delta = fmaf(Elem<T>::to_f32(e8[e]), __uint_as_float(o[q * 8 + e]) * inv, delta);
-          }
-        }
-        if (n_tiles > 0) {
-          if (write_y) {
-            if ((c & 1) == 0) {
-              // the warp's previous store has finished reading the staging buffer
-              if (lane == 0) bulk_wait_read<0>();
-              __syncwarp();
-            }
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t wv[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const float v0 = __uint_as_float(o[q * 8 + 2 * e]) * inv;
-                const float v1 = __uint_as_float(o[q * 8 + 2 * e + 1]) * inv;
-                wv[e] = kBF16 ? pack_bf16x2(v0, v1) : pack_f16x2(v0, v1);
-              }
-              const int c16 = (c & 1) * 4 + q;   // 16-byte piece of the row within the 64 columns
-              if (SDPA_IN_BOUNDS(lane * 128 + (c16 << 4) + 16 <= C::kYWarpBytes || kStage, 104))
-                st_shared_v4(sY + lane * 128 + ((c16 ^ (lane & 7)) << 4), wv[0], wv[1], wv[2], wv[3]);
-            }
-            if ((c & 1) == 1) {
-              fence_proxy_async_smem();
-              __syncwarp();
-              // a warp whose rows all lie past S has nothing to store
-              if (lane == 0 && mx0 + sub * 32 < a.S && SDPA_IN_BOUNDS(mx0 + sub * 32 >= 0, 105)) {
-                tma_store_4d(&ty, sY, (c >> 1) * 64, yc1, yc2, yc3);
-                bulk_commit();
-              }
-            }
-          }
-        } else if (valid && write_y) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            uint32_t wv[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float v0 = __uint_as_float(o[q * 8 + 2 * e]) * inv;
-              const float v1 = __uint_as_float(o[q * 8 + 2 * e + 1]) * inv;
-              wv[e] = kBF16 ? pack_bf16x2(v0, v1) : pack_f16x2(v0, v1);
-            }
-            *reinterpret_cast<uint4*>(yrow + c * 32 + q * 8) = make_uint4(wv[0], wv[1], wv[2], wv[3]);
-          }
-        }
-      }
-      if (stats && valid) {
-        const int64_t r_idx = ((int64_t)b * a.Nq + qh) * a.S + i;
-        a.lse2_out[r_idx] = (denom > 0.f && m_use != -INFINITY) ? m_use + log2f(denom) : INFINITY;
-        a.delta_out[r_idx] = delta;
-      }
-      // the epilogue's tensor-memory reads are complete before this thread's next P store,
-      // which the MMA warp waits for before the next unit's first PV overwrites O
+      // the epilogue of this unit runs at the top of the next pass
+      e_real = true;
+      e_tiles = n_tiles;
+      e_l = l;
+      e_m = m_use;
+      e_valid = valid;
+      e_i = i;
+      e_b = b;
+      e_qh = qh;
+      e_mx0 = mx0;
     }
     // the warp's last stores have read shared memory before the CTA exits
     if (lane == 0) bulk_wait_all();
