@@ -7,8 +7,8 @@
 // 128-row query tiles that stream the same key/value tiles: two query heads of one GQA group
 // over one row block, or two consecutive row blocks of one head.
 //
-//   warp 0      TMA producer: the unit's Q tiles (once the previous unit's last S MMAs have
-//               read the buffer), then K_0, V_0, K_1, V_1, ... into the ring
+//   warp 0      TMA producer: the unit's first K tile, its Q tiles (once the previous unit's
+//               last S MMAs have read the buffer), then V_0, K_1, V_1, ... into the ring
 //   warp 1      MMA issuer (the whole warp runs the loop, one elected lane issues):
 //               S_X = Q_X K_j^T into TMEM, O_X += P_X V_j with P read from TMEM
 //   warps 4-7   softmax of tile 0: each thread owns one query row (TMEM lane = row)
@@ -17,8 +17,9 @@
 // The two softmax warpgroups alternate with the tensor core: while one works on its
 // scores the MMA warp computes the other's products.  Running maxima are kept in the
 // base-2 domain and only moved (with a rescale of the TMEM accumulator) when they grow
-// by more than 2^8, so most tiles skip the rescale.  At the end of a unit each softmax warp
-// stages its rows of y in shared memory and writes them with TMA stores.
+// by more than 2^8, so most tiles skip the rescale.  A unit's epilogue (each softmax warp
+// stages its rows of y in shared memory and writes them with TMA stores) runs at the top of
+// the warp's next pass over the unit list; before the first unit the same code runs once dry.
 //
 // Every barrier wait is bounded: on expiry the kernel raises an abort flag, drains the
 // copies and MMAs it issued, frees its tensor memory and records SDPA_ERR_TIMEOUT in a
@@ -44,8 +45,9 @@ using namespace ptx;
 
 constexpr int kBM = 128;        // query rows per tile (TMEM lanes)
 constexpr int kBN = 128;        // keys per tile
-// CTA shape for QT 128-row query tiles per CTA (1: two CTAs share an SM; 2: one CTA) and
-// SPLIT softmax threads per query row (each owns 128 / SPLIT score columns of a key tile).
+// CTA shape for QT 128-row query tiles per CTA and SPLIT softmax threads per query row (each
+// owns 128 / SPLIT score columns of a key tile).  The kernel instantiates QT = 2 (one CTA per
+// SM) and SPLIT = 1.
 template <int QT, int SPLIT>
 struct Layout {
   static constexpr int kSmxThreads = 128 * QT * SPLIT;    // softmax warpgroups
